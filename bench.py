@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the paged attention hot path on GB300.
+
+One step = one paged_attn_mixed call (row routing, then the prefill kernel;
+rows short enough for the decode path would also run split-KV decode + merge)
+over the varlen causal prefill workload: 8 rows, new query lengths uniform in
+[65, 2048], prior cached context uniform in [0, 16384], 32 query / 8 KV heads,
+head dim 128, pages of 16 tokens, bf16, shuffled block table (seed 20262).
+The headline value is prefill TFLOP/s by the visible-pair FLOP convention.
+The decode half of the metric (KV GB/s) is measured on the split-KV decode
+batch (256 rows, L up to 32768) and the long-context fp8 decode batch, and
+reported under "parts" with the mixed batch and the small decode batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(rows are independent: weak scaling, no data-path collective).  The
+reference arm (--impl reference) times the fp64 CPU oracle on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import datetime as _dt
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_attention_prefill_gb300 import dist as padist  # noqa: E402
+from paged_kv_attention_prefill_gb300 import metrics, workloads  # noqa: E402
+
+METRIC = "prefill TFLOPS & decode KV GB/s (fraction of GB300 roofline), 1 GPU"
+HEADLINE_WORKLOAD = 2
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.sel = str(device_index)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(f):
+                if len(r) < 9:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                rows.append((ts, [x.strip() for x in r[1:]]))
+        os.unlink(self.path)
+        inside = [x for t, x in rows if self.t0 is not None and self.t0 <= t <= self.t1 + 0.05]
+        note = "inside timed region"
+        if not inside:
+            inside = [x for _, x in rows]
+            note = "timed region shorter than the sampling interval: all samples of the run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(x[0]) for x in inside if x[0].replace(".", "").isdigit()]
+        mx = [float(x[1]) for x in inside if x[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for x in inside for i in range(4) if x[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def launches_per_call(q_lens, max_dq=16):
+    dec = any(1 <= q <= max_dq for q in q_lens)
+    pre = any(q > max_dq for q in q_lens)
+    return 1 + (2 if dec else 0) + (1 if pre else 0)
+
+
+def call_args(b):
+    return dict(cu_seqlens_q_host=b.cu_seqlens_q.cpu(), seq_lens_host=b.seq_lens.cpu(),
+                softmax_scale=b.softmax_scale, k_scale=b.k_scale, v_scale=b.v_scale)
+
+
+def time_calls(fn, steps, warmup, stream, sampler=None):
+    """Times exactly `steps` calls with CUDA events on the launching stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    padist.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark("t0")
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    padist.barrier()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def part_decode(n, steps, warmup, stream, pk):
+    import paged_kv_attention_prefill_gb300 as pa
+    b = workloads.make_workload(n, device="cuda", data_device="cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+
+    def fn():
+        pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                             b.seq_lens, out=out, workspace=ws, **kw)
+    ms = time_calls(fn, steps, warmup, stream)
+    byt = metrics.decode_bytes(b.q_lens, b.kv_lens, num_q_heads=b.num_q_heads,
+                               num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+                               q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, page_size=b.page_size)
+    gbs = byt / (ms * 1e-3) / 1e9
+    res = {"workload": workloads.WORKLOADS[n], "ms": round(ms, 4), "kv_bytes": byt,
+           "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+           "launches_per_call": 2}
+    del b, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def part_mixed3(steps, warmup, stream, pk):
+    import paged_kv_attention_prefill_gb300 as pa
+    b = workloads.make_workload(3, device="cuda", data_device="cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+
+    def fn():
+        pa.paged_attn_mixed(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                            b.seq_lens, out=out, workspace=ws, **kw)
+    ms = time_calls(fn, steps, warmup, stream)
+    ql, kl = b.q_lens, b.kv_lens
+    F = metrics.prefill_flops(ql[:1], kl[:1], b.num_q_heads, b.head_dim)
+    byt = metrics.decode_bytes(ql[1:], kl[1:], num_q_heads=b.num_q_heads,
+                               num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+                               q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, page_size=b.page_size)
+    res = {"workload": workloads.WORKLOADS[3], "ms": round(ms, 4), "prefill_flops": F,
+           "decode_bytes": byt, "whole_call_TFLOP/s_of_prefill": round(F / (ms * 1e-3) / 1e12, 1),
+           "launches_per_call": launches_per_call(ql)}
+    del b, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
+def part_small1(steps, warmup, stream):
+    import paged_kv_attention_prefill_gb300 as pa
+    b = workloads.make_workload(1).to("cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+
+    def fn():
+        pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                             b.seq_lens, out=out, workspace=ws, **kw)
+    ms = time_calls(fn, steps, warmup, stream)
+    return {"workload": workloads.WORKLOADS[1], "us_per_call": round(ms * 1e3, 2),
+            "note": "launch-latency bound (0.59 MB)"}
+
+
+def cpu_baseline_sample(b, budget_s=12.0):
+    """Times the oracle on sampled query tokens of the workload; returns
+    (TFLOP/s, cores, description)."""
+    import oracle
+    cpu = b.to("cpu")
+    args = cpu.oracle_args()
+    ql, kl = cpu.q_lens, cpu.kv_lens
+    cu = [0]
+    for q in ql:
+        cu.append(cu[-1] + q)
+    # one token from the end of each row (the most keys), scaled up to the budget
+    pool = []
+    for r, q in enumerate(ql):
+        for i in range(q - 1, -1, -max(1, q // 64)):
+            pool.append((cu[r] + i, kl[r] - q + i + 1))
+    pool.sort(key=lambda x: x[0])
+    probe = pool[:: max(1, len(pool) // 8)][:8]
+    t = time.perf_counter()
+    oracle.paged_attention(tokens=[x[0] for x in probe], **args)
+    dt = time.perf_counter() - t
+    fl_probe = sum(4 * cpu.head_dim * cpu.num_q_heads * k for _, k in probe)
+    rate = fl_probe / max(dt, 1e-6)
+    want = rate * budget_s
+    pick, acc = [], 0
+    for x in pool[:: max(1, len(pool) // 4096)]:
+        if acc >= want:
+            break
+        pick.append(x)
+        acc += 4 * cpu.head_dim * cpu.num_q_heads * x[1]
+    t = time.perf_counter()
+    oracle.paged_attention(tokens=[x[0] for x in pick], **args)
+    dt = time.perf_counter() - t
+    return acc / dt / 1e12, oracle.num_threads(), \
+        f"{len(pick)} query tokens x {cpu.num_q_heads} heads of the workload ({acc:.3e} FLOP, {dt:.1f} s)"
+
+
+def run_ours(args):
+    import paged_kv_attention_prefill_gb300 as pa
+    from paged_kv_attention_prefill_gb300 import build as pa_build
+    rank, world, local = padist.env_rank_world()
+    torch.cuda.set_device(local)
+    padist.init("nccl")
+    pa_build.build()
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    b = workloads.make_workload(HEADLINE_WORKLOAD, device="cuda", data_device="cuda",
+                                page_size=16)
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+    ql, kl = b.q_lens, b.kv_lens
+    F = metrics.prefill_flops(ql, kl, b.num_q_heads, b.head_dim)
+
+    def step():
+        pa.paged_attn_mixed(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                            b.seq_lens, out=out, workspace=ws, **kw)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ms_local = time_calls(step, args.steps, args.warmup, stream, sampler)
+    clocks = sampler.stop() if sampler else None
+    ms = padist.max_over_ranks(ms_local, device="cuda")
+    total_flops = F * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    achieved = F / (ms_local * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers
+    in_bytes = sum(t.numel() * t.element_size() for t in
+                   (b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens))
+    host = {k: getattr(b, k).cpu().pin_memory() for k in
+            ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seq_lens")}
+    dev = {k: torch.empty_like(getattr(b, k)) for k in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        pa.paged_attn_mixed(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
+                            dev["cu_seqlens_q"], dev["seq_lens"], out=out, workspace=ws, **kw)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    ms_e2e = padist.max_over_ranks(time_calls(e2e_step, e2e_steps, 2, stream), device="cuda")
+    e2e_val = total_flops / (ms_e2e * 1e-3) / 1e12
+    del host, dev
+    torch.cuda.empty_cache()
+
+    res = None
+    if rank == 0:
+        parts = {}
+        if not args.headline_only:
+            ps, pw = max(5, min(args.steps, 30)), 3
+            parts["decode_split_kv_256rows"] = part_decode(4, ps, pw, stream, pk)
+            parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk)
+            parts["mixed_chunk_plus_decode"] = part_mixed3(ps, pw, stream, pk)
+            parts["decode_small_4rows"] = part_small1(max(ps, 50), 5, stream)
+        cpu_val, cores, sample = cpu_baseline_sample(b, budget_s=args.cpu_seconds)
+        res = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16, shuffled block tables, poisoned unused slots)",
+            "config": {"workload": workloads.WORKLOADS[HEADLINE_WORKLOAD], "rows": b.num_rows,
+                       "q_lens": ql, "kv_lens": kl, "page_size": 16,
+                       "flops_per_step": F, "entry": "paged_attn_mixed",
+                       "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush",
+                       "parallelism": f"replicas x{world} (rows independent)"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(achieved / pk["bf16"], 4), "traffic": None,
+                         "kernel": "prefill (whole call timed: routing kernel included)",
+                         "peak_source": f"{pk['source']} bf16 burst"},
+            "cpu_baseline": {"value": round(cpu_val, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 3),
+                    "h2d_bytes_per_step": in_bytes,
+                    "d2h_bytes_per_step": out.numel() * out.element_size()},
+            "gpu_launches": launches_per_call(ql) * args.steps,
+            "clocks": clocks,
+            "parts": parts,
+        }
+        print(json.dumps(res), flush=True)
+    padist.barrier()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = padist.env_rank_world()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    b = workloads.make_workload(HEADLINE_WORKLOAD, page_size=16)
+    budget = max(0.5, args.ref_seconds)
+    vals, descr, cores = [], "", oracle.num_threads()
+    for s in range(args.warmup + args.steps):
+        v, cores, descr = cpu_baseline_sample(b, budget_s=budget)
+        if s >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    F = metrics.prefill_flops(b.q_lens, b.kv_lens, b.num_q_heads, b.head_dim)
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(F / (value * 1e12) * 1e3, 3) if value > 0 else None,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": workloads.WORKLOADS[HEADLINE_WORKLOAD],
+                                            "page_size": 16, "flops_per_step": F},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                            "kind": "oracle",
+                            "sample": f"per step: {descr}; ms_per_step extrapolates to the whole workload"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=4.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * paged_attn.h -- attention over a paged (block-table) KV cache on GB300
+ * (sm_103a): varlen causal paged prefill, split-KV paged decode, and a mixed
+ * call that routes each row of a serving batch to one of the two.
+ *
+ * Plain C ABI: every argument is a plain pointer (host or device, as stated)
+ * or a size; no C++ or framework types cross it.  The library never allocates
+ * or frees memory and never synchronizes the stream inside a compute call.
+ *
+ * ------------------------------------------------------------------------
+ * The operation (all three compute entry points compute the same thing)
+ * ------------------------------------------------------------------------
+ * A batch holds num_rows sequences ("rows").  Row b brings q_b new query
+ * tokens, q_b = cu_seqlens_q[b+1] - cu_seqlens_q[b], packed one row after
+ * another in q; its KV length L_b = seq_lens[b] counts every key of the row,
+ * the new tokens included, so the new tokens are the LAST q_b keys (bottom-
+ * right causal alignment).  Query token i of row b (0 <= i < q_b) in query
+ * head h attends to keys j = 0 .. L_b - q_b + i of KV head h / (Hq / Hkv):
+ *
+ *     x_j = s * (q . k_j) * k_scale,   out = sum_j softmax(x)_j * v_j * v_scale
+ *
+ * Key j of row b is slot j % P of physical page block_table[b][j / P].
+ * A token with no visible key (L_b - q_b + i < 0; in particular every token of
+ * a row with L_b = 0, an empty row) produces exact zeros.
+ *
+ * Sources: vllm-rlt PR #128 ("Purpose": the packed interface with
+ * cu_seqlens_q, one block table per sequence, bottom-right causal alignment,
+ * tiles with online softmax, K/V gathered through the block table, GQA; the
+ * split-KV decode with 16 equal tile-aligned parts per row, fp32 partial
+ * softmax states merged by a second kernel, a partition that depends on the
+ * row's own length only, a static grid; "Memory": the fp32 workspace of
+ * rows x heads x 16 x (head_dim + 2) x 4 bytes).  1Cat-vLLM PR #616 (original
+ * description, "Purpose": small-query rows -- q = 1 decode and q = K+1
+ * speculative-verify rows -- sent to the paged decode kernel instead of the
+ * per-sequence prefill loop; the page size as a kernel argument, any
+ * multiple of 16, with bit-identical results; an fp8_e5m2 KV cache).
+ * 1Cat-vLLM PR #1279 (commit 1: GQA-packed query rows per CTA; commit 5:
+ * key-range splits merged by log-sum-exp).
+ *
+ * ------------------------------------------------------------------------
+ * Layouts (all row-major and contiguous)
+ * ------------------------------------------------------------------------
+ *   q, out        [total_q, Hq, head_dim]      element type q_dtype
+ *   k_cache,
+ *   v_cache       [num_pages, page_size, Hkv, head_dim]   element type kv_dtype
+ *                 (PA_E5M2: one byte per element)
+ *   block_table   int32 [num_rows, max_pages_per_row]; entries past a row's
+ *                 ceil(L_b / P) pages are never read
+ *   cu_seqlens_q  int32 [num_rows + 1], non-decreasing, cu_seqlens_q[0] = 0
+ *   seq_lens      int32 [num_rows]
+ * Query head h uses KV head h / (Hq / Hkv) (consecutive query heads share a
+ * KV head).  Byte offsets into the caches are 64-bit.
+ *
+ * ------------------------------------------------------------------------
+ * Ownership, streams and errors
+ * ------------------------------------------------------------------------
+ * All buffers are caller-owned.  q, caches, tables and workspace are device
+ * memory; out is device memory and is fully written (every token of every
+ * row).  The *_host mirrors in pa_batch are optional host copies; when given
+ * they are used for argument checks and tighter grids (never stored).
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  They keep no state between calls except a per-device cache of
+ * launch attributes, and are safe to call from several host threads with
+ * distinct workspaces.  Results are deterministic: the same call gives the
+ * same bits; a row's output does not depend on the other rows of the batch,
+ * on the page size or on which physical pages hold it.
+ *
+ * Every entry point returns a pa_status.  Host-detectable problems
+ * (null pointers, bad sizes, unsupported types, a small workspace, and --
+ * when host mirrors are given -- negative lengths, L_b > max_pages_per_row * P
+ * or a decode row with q_b > max_decode_q) return an error before any launch.
+ * Problems only the device can see (without host mirrors: a block-table entry
+ * outside [0, num_pages) for a page that is needed, a row longer than its
+ * block-table row, a decode row with q_b > max_decode_q) are never
+ * dereferenced: such a slot reads as zeros, such a row is skipped, and a
+ * sticky flag is set in the workspace header, readable with
+ * paged_attn_read_errors().
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,          /* null pointer, inconsistent sizes or lengths */
+  PA_ERR_UNSUPPORTED = 2,          /* head_dim / dtype combination not built */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < paged_attn_workspace_size() */
+  PA_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed */
+  PA_ERR_NO_DEVICE = 5             /* no sm_103 device is current */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_F32 = 0,
+  PA_F16 = 1,
+  PA_BF16 = 2,
+  PA_E5M2 = 3   /* fp8 E5M2 (KV cache only), value = code * scale */
+} pa_dtype;
+
+/* Problem parameters.  Zero-initialise, then set what you need. */
+typedef struct pa_params {
+  int32_t num_q_heads;    /* Hq > 0 */
+  int32_t num_kv_heads;   /* Hkv > 0, Hq % Hkv == 0 */
+  int32_t head_dim;       /* 64, 128 or 256 */
+  int32_t page_size;      /* P > 0 and a multiple of 16 */
+  int32_t q_dtype;        /* pa_dtype of q and out: PA_BF16, PA_F16 or PA_F32 */
+  int32_t kv_dtype;       /* pa_dtype of the caches: same as q_dtype, or PA_E5M2
+                             with a 16-bit q_dtype */
+  float softmax_scale;    /* s; 0 selects 1/sqrt(head_dim) */
+  float k_scale;          /* per-tensor scale of K; 0 selects 1 */
+  float v_scale;          /* per-tensor scale of V; 0 selects 1 */
+  int32_t max_decode_q;   /* mixed: rows with 1 <= q_b <= max_decode_q go to the
+                             split-KV decode path; 0 selects 16.  decode: the
+                             largest q_b allowed. */
+  int32_t num_splits;     /* split-KV parts per decode row: 0 or 16 */
+} pa_params;
+
+typedef struct pa_batch {
+  int32_t num_rows;             /* B >= 0 */
+  int32_t total_q;              /* cu_seqlens_q[B], the rows of q and out */
+  int32_t num_pages;            /* pages in each cache */
+  int32_t max_pages_per_row;    /* columns of block_table */
+  const int32_t* cu_seqlens_q;  /* device [B + 1] */
+  const int32_t* seq_lens;      /* device [B] */
+  const int32_t* block_table;   /* device [B, max_pages_per_row] */
+  const int32_t* cu_seqlens_q_host;  /* optional host mirror [B + 1] (or NULL) */
+  const int32_t* seq_lens_host;      /* optional host mirror [B] (or NULL) */
+} pa_batch;
+
+/*
+ * Bytes of device workspace the three compute calls need for a batch of at
+ * most num_rows rows and total_q query tokens (an upper bound, so one buffer
+ * serves every batch up to those sizes).  It holds a 256-byte header (error
+ * flags, work counts), the mixed call's row plan, and the fp32 split-KV
+ * partial states, (acc[d], m, l) per decode token, query head and split --
+ * the vllm-rlt PR #128 "Memory" figure of heads x 16 x (head_dim + 2) x 4
+ * bytes per decode token.  Returns 0 for invalid parameters.
+ * The workspace must be zero-filled once before its first use (the header's
+ * error word is sticky); the calls never require it to be zeroed again.
+ */
+size_t paged_attn_workspace_size(const pa_params* params, int32_t num_rows, int32_t total_q);
+
+/*
+ * Varlen causal paged prefill: every row with q_b > 0, whatever its length,
+ * on the prefill kernel (GQA-packed query tiles, online softmax over key
+ * tiles, bottom-right causal mask).  Short rows are correct but slow here;
+ * use paged_attn_mixed for serving batches.
+ */
+pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, const void* q,
+                             const void* k_cache, const void* v_cache, void* out,
+                             void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Split-KV paged decode: every row (1 <= q_b <= max_decode_q; q_b > 1 are
+ * speculative-verify rows) split into num_splits (16) contiguous parts of
+ * whole 64-key tiles, chosen from L_b alone; one CTA per (row, 16-row block
+ * of GQA-packed query rows, KV head, split) writes fp32 partial states; a
+ * second kernel merges them in fixed split order.  Batch-invariant bitwise.
+ */
+pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, const void* q,
+                            const void* k_cache, const void* v_cache, void* out,
+                            void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * Mixed serving batch: rows with 1 <= q_b <= max_decode_q go to the split-KV
+ * decode path, longer rows to the prefill kernel, rows with q_b = 0 are
+ * skipped.  The routing is computed on the device from cu_seqlens_q, so the
+ * call needs no host mirrors and its grids depend only on num_rows and
+ * total_q (capturable in a CUDA graph).  Each token's result is bitwise equal
+ * to the one the corresponding single-path call gives.
+ */
+pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const void* q,
+                           const void* k_cache, const void* v_cache, void* out,
+                           void* workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* Error flags the kernels may set in the workspace header (sticky). */
+#define PA_DEVERR_BAD_PAGE   0x1u  /* a needed block-table entry outside [0, num_pages),
+                                      or a key past the row's block-table columns */
+#define PA_DEVERR_DECODE_Q   0x4u  /* a decode-path row with q_b > max_decode_q */
+
+/*
+ * Copies the workspace header's error flags to *flags (host) and clears
+ * them.  Synchronizes `stream`.  Not a compute call.
+ */
+pa_status paged_attn_read_errors(void* workspace, pa_stream_t stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* paged_attn_status_string(pa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t paged_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

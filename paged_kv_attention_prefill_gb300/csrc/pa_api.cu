@@ -1,0 +1,309 @@
+// C ABI of the paged attention library: argument checks, workspace layout,
+// routing and launches.  No allocation, no stream synchronization.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+
+#include "pa_internal.cuh"
+
+namespace pa {
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static int64_t max_tiles_for(int num_rows, int total_q, int g, int bm) {
+  return ((int64_t)total_q * g + bm - 1) / bm + num_rows;
+}
+
+WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g) {
+  WsLayout w{};
+  w.max_slots = std::min<int64_t>(total_q, (int64_t)num_rows * max_decode_q);
+  w.max_tiles = max_tiles_for(num_rows, total_q, g, 16);  // the smallest tile height in use
+  size_t off = sizeof(WsHeader);
+  w.dec_base = off;
+  off += align_up((size_t)num_rows * 4, 256);
+  w.slot_tok = off;
+  off += align_up((size_t)w.max_slots * 4, 256);
+  w.tiles = off;
+  off += align_up((size_t)w.max_tiles * 8, 256);
+  w.part_ml = off;
+  off += align_up((size_t)w.max_slots * hq * NSPLIT * 8, 256);
+  w.part_acc = off;
+  off += (size_t)w.max_slots * hq * NSPLIT * d * 4;
+  w.total = align_up(off, 256);
+  return w;
+}
+
+namespace {
+
+struct Resolved {
+  int hq, hkv, g, d, P;
+  int qd, kvd;
+  float scale, k_scale, v_scale;
+  int max_dq;
+  bool host;          // host mirrors present
+  int host_max_q_dec; // mixed/decode: largest q_b among decode rows (host mirrors)
+  int host_tiles;     // prefill work items (host mirrors), for the tile height in use
+  int host_slots;     // decode slots (host mirrors)
+};
+
+// 0 = not checked, 1 = sm_103, 2 = other
+std::atomic<uint8_t> g_dev_ok[64];
+
+pa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_NO_DEVICE;
+  const int slot = dev & 63;
+  uint8_t s = g_dev_ok[slot].load(std::memory_order_acquire);
+  if (s == 0) {
+    int maj = 0, min = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return PA_ERR_NO_DEVICE;
+    s = (maj == 10 && min == 3) ? 1 : 2;
+    g_dev_ok[slot].store(s, std::memory_order_release);
+  }
+  return s == 1 ? PA_OK : PA_ERR_NO_DEVICE;
+}
+
+pa_status resolve_params(const pa_params* prm, Resolved* r) {
+  if (!prm) return PA_ERR_INVALID_ARG;
+  if (prm->num_q_heads <= 0 || prm->num_kv_heads <= 0 ||
+      prm->num_q_heads % prm->num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (prm->page_size <= 0 || prm->page_size % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (prm->head_dim <= 0) return PA_ERR_INVALID_ARG;
+  if (prm->head_dim != 64 && prm->head_dim != 128 && prm->head_dim != 256)
+    return PA_ERR_UNSUPPORTED;
+  const int qd = prm->q_dtype, kvd = prm->kv_dtype;
+  if (qd != PA_BF16 && qd != PA_F16 && qd != PA_F32) return PA_ERR_UNSUPPORTED;
+  if (!(kvd == qd || (kvd == PA_E5M2 && qd != PA_F32))) return PA_ERR_UNSUPPORTED;
+  if (prm->num_splits != 0 && prm->num_splits != NSPLIT) return PA_ERR_UNSUPPORTED;
+  if (prm->max_decode_q < 0) return PA_ERR_INVALID_ARG;
+  if (!(std::isfinite(prm->softmax_scale) && std::isfinite(prm->k_scale) &&
+        std::isfinite(prm->v_scale)))
+    return PA_ERR_INVALID_ARG;
+  r->hq = prm->num_q_heads;
+  r->hkv = prm->num_kv_heads;
+  r->g = r->hq / r->hkv;
+  r->d = prm->head_dim;
+  r->P = prm->page_size;
+  r->qd = qd;
+  r->kvd = kvd;
+  r->scale = prm->softmax_scale != 0.f ? prm->softmax_scale : 1.f / std::sqrt((float)r->d);
+  r->k_scale = prm->k_scale != 0.f ? prm->k_scale : 1.f;
+  r->v_scale = prm->v_scale != 0.f ? prm->v_scale : 1.f;
+  r->max_dq = prm->max_decode_q ? prm->max_decode_q : 16;
+  return PA_OK;
+}
+
+enum Entry { E_PREFILL, E_DECODE, E_MIXED };
+
+pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const void* q,
+                   const void* kc, const void* vc, void* out, void* ws, size_t ws_bytes,
+                   Resolved* r) {
+  pa_status s = resolve_params(prm, r);
+  if (s != PA_OK) return s;
+  if (!bat || bat->num_rows < 0 || bat->total_q < 0 || bat->num_pages < 0 ||
+      bat->max_pages_per_row < 0)
+    return PA_ERR_INVALID_ARG;
+  if (!ws) return PA_ERR_INVALID_ARG;
+  if (bat->num_rows > 0) {
+    if (!bat->cu_seqlens_q || !bat->seq_lens || !bat->block_table) return PA_ERR_INVALID_ARG;
+    if (bat->max_pages_per_row <= 0 || bat->num_pages <= 0) return PA_ERR_INVALID_ARG;
+  }
+  if (bat->total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
+  if (bat->num_rows > 0 && (!kc || !vc)) return PA_ERR_INVALID_ARG;
+  if ((int64_t)bat->total_q * r->g > INT32_MAX / 2) return PA_ERR_INVALID_ARG;
+  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g);
+  if (ws_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+  r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
+  r->host_max_q_dec = 0;
+  r->host_tiles = 0;
+  r->host_slots = 0;
+  if (r->host) {
+    const int32_t* cu = bat->cu_seqlens_q_host;
+    const int32_t* lens = bat->seq_lens_host;
+    if (bat->num_rows > 0 && cu[0] != 0) return PA_ERR_INVALID_ARG;
+    if (cu[bat->num_rows] != bat->total_q) return PA_ERR_INVALID_ARG;
+    const int bm = r->qd == PA_F32 ? 16 : PF_BM;
+    for (int b = 0; b < bat->num_rows; ++b) {
+      const int qb = cu[b + 1] - cu[b];
+      const int L = lens[b];
+      if (qb < 0 || L < 0) return PA_ERR_INVALID_ARG;
+      if ((int64_t)L > (int64_t)bat->max_pages_per_row * r->P) return PA_ERR_INVALID_ARG;
+      const bool dec = entry == E_DECODE || (entry == E_MIXED && qb >= 1 && qb <= r->max_dq);
+      if (entry == E_DECODE && qb > r->max_dq) return PA_ERR_INVALID_ARG;
+      if (dec) {
+        r->host_max_q_dec = std::max(r->host_max_q_dec, qb);
+        r->host_slots += qb;
+      } else if (qb > 0) {
+        r->host_tiles += (qb * r->g + bm - 1) / bm;
+      }
+    }
+  }
+  return check_device();
+}
+
+AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const void* kc,
+                   const void* vc, void* out, void* ws) {
+  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  AttnArgs a{};
+  a.p.cu_q = bat->cu_seqlens_q;
+  a.p.seq_lens = bat->seq_lens;
+  a.p.bt = bat->block_table;
+  a.p.num_rows = bat->num_rows;
+  a.p.total_q = bat->total_q;
+  a.p.max_pages = bat->max_pages_per_row;
+  a.p.num_pages = bat->num_pages;
+  a.p.page_size = r.P;
+  a.p.hq = r.hq;
+  a.p.hkv = r.hkv;
+  a.p.g = r.g;
+  a.p.d = r.d;
+  a.p.sl2 = r.scale * r.k_scale * 1.4426950408889634f;
+  a.p.v_scale = r.v_scale;
+  a.p.err = reinterpret_cast<uint32_t*>(base);
+  a.q = q;
+  a.kc = kc;
+  a.vc = vc;
+  a.out = out;
+  a.part_acc = reinterpret_cast<float*>(base + w.part_acc);
+  a.part_ml = reinterpret_cast<float2*>(base + w.part_ml);
+  a.dec_base = nullptr;
+  a.slot_tok = nullptr;
+  a.tiles = reinterpret_cast<const int2*>(base + w.tiles);
+  a.n_tiles = &reinterpret_cast<const WsHeader*>(base)->n_tiles;
+  a.max_decode_q = r.max_dq;
+  a.max_slots = w.max_slots;
+  return a;
+}
+
+inline pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+int decode_mblocks(const Resolved& r, int max_q) {
+  return (max_q * r.g + DEC_ROWS - 1) / DEC_ROWS;
+}
+
+// Launches the decode CTAs and the merge for the rows routed to decode.
+cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_slots,
+                       cudaStream_t st) {
+  AttnArgs a = a0;
+  a.dec_mblk = n_mblk;
+  cudaError_t e;
+  if (r.qd == PA_F32)
+    e = launch_f32(a, 1, 0, n_mblk, st);
+  else
+    e = launch_decode_mma(a, r.qd, r.kvd, n_mblk, st);
+  if (e != cudaSuccess) return e;
+  return launch_merge(a, r.qd, n_slots, st);
+}
+
+cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, cudaStream_t st) {
+  if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
+  return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+size_t paged_attn_workspace_size(const pa_params* params, int32_t num_rows, int32_t total_q) {
+  Resolved r;
+  if (resolve_params(params, &r) != PA_OK || num_rows < 0 || total_q < 0) return 0;
+  return workspace_layout(num_rows, total_q, r.hq, r.d, r.max_dq, r.g).total;
+}
+
+pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, const void* q,
+                             const void* k_cache, const void* v_cache, void* out,
+                             void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  Resolved r;
+  pa_status s = validate(E_PREFILL, params, batch, q, k_cache, v_cache, out, workspace,
+                         workspace_bytes, &r);
+  if (s != PA_OK) return s;
+  if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
+  const int bm = r.qd == PA_F32 ? 16 : PF_BM;
+  const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
+  cudaError_t e = launch_plan(a, 0, 0, bm, max_tiles, st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  const int grid = r.host ? r.host_tiles : max_tiles;
+  return cuda_status(run_prefill(a, r, grid, st));
+}
+
+pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, const void* q,
+                            const void* k_cache, const void* v_cache, void* out,
+                            void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  Resolved r;
+  pa_status s = validate(E_DECODE, params, batch, q, k_cache, v_cache, out, workspace,
+                         workspace_bytes, &r);
+  if (s != PA_OK) return s;
+  if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
+  const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
+  const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
+  return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots, st));
+}
+
+pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const void* q,
+                           const void* k_cache, const void* v_cache, void* out,
+                           void* workspace, size_t workspace_bytes, pa_stream_t stream) {
+  Resolved r;
+  pa_status s = validate(E_MIXED, params, batch, q, k_cache, v_cache, out, workspace,
+                         workspace_bytes, &r);
+  if (s != PA_OK) return s;
+  if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
+  const WsLayout w = workspace_layout(batch->num_rows, batch->total_q, r.hq, r.d, r.max_dq, r.g);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  a.dec_base = reinterpret_cast<const int32_t*>(base + w.dec_base);
+  a.slot_tok = reinterpret_cast<const int32_t*>(base + w.slot_tok);
+  const int bm = r.qd == PA_F32 ? 16 : PF_BM;
+  const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
+  cudaError_t e = launch_plan(a, 1, r.max_dq, bm, max_tiles, st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  // decode rows: the grid covers every row; rows routed to prefill exit at once
+  const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
+  const int n_slots = r.host ? r.host_slots : (int)a.max_slots;
+  if (max_q > 0) {
+    e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, st);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  const int grid = r.host ? r.host_tiles : max_tiles;
+  return cuda_status(run_prefill(a, r, grid, st));
+}
+
+pa_status paged_attn_read_errors(void* workspace, pa_stream_t stream, uint32_t* flags) {
+  if (!workspace || !flags) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, 4, st) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  *flags = v;
+  return PA_OK;
+}
+
+const char* paged_attn_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported head_dim or dtype combination";
+    case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_NO_DEVICE: return "no sm_103 device is current";
+  }
+  return "unknown status";
+}
+
+int32_t paged_attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// Row plan (the mixed call's router), the split-KV merge, and the fp32 path.
+#include "pa_internal.cuh"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Plan: classify rows and lay out the work of one call (one CTA).
+//
+// Mixed mode (1Cat-vLLM PR #616, original description, "Purpose": short
+// decode and speculative-verify rows are routed to a single paged-decode
+// launch and left out of the prefill work): a row with 1 <= q_b <= max_decode_q gets
+// q_b consecutive decode slots (its partial states); every other row with
+// q_b > 0 gets ceil(q_b * g / bm) prefill work items.  Prefill-only mode
+// sends every row with q_b > 0 to the prefill list.  Work items of a row are
+// listed last block first (the blocks with the most visible keys first).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed, int max_dq,
+                                                    int bm, WsHeader* hdr, int32_t* dec_base,
+                                                    int32_t* slot_tok, int2* tiles, int max_tiles,
+                                                    int64_t max_slots) {
+  __shared__ int s_tiles[1024], s_slots[1024];
+  __shared__ int s_tot_tiles, s_tot_slots;
+  const Problem& p = a.p;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_tot_tiles = 0;
+    s_tot_slots = 0;
+  }
+  __syncthreads();
+  for (int c0 = 0; c0 < p.num_rows; c0 += 1024) {
+    const int b = c0 + tid;
+    int qb = 0, qs = 0;
+    if (b < p.num_rows) {
+      qs = p.cu_q[b];
+      qb = p.cu_q[b + 1] - qs;
+    }
+    if (qs < 0 || qs + qb > p.total_q) qb = 0;  // malformed row: the kernels skip it too
+    const bool dec = mixed && qb >= 1 && qb <= max_dq;
+    const int nt = (!dec && qb > 0) ? (qb * p.g + bm - 1) / bm : 0;
+    const int ns = dec ? qb : 0;
+    s_tiles[tid] = nt;
+    s_slots[tid] = ns;
+    __syncthreads();
+    // inclusive Hillis-Steele scan over the chunk
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int vt = tid >= off ? s_tiles[tid - off] : 0;
+      const int vs = tid >= off ? s_slots[tid - off] : 0;
+      __syncthreads();
+      s_tiles[tid] += vt;
+      s_slots[tid] += vs;
+      __syncthreads();
+    }
+    const int t_off = s_tot_tiles + s_tiles[tid] - nt;
+    const int s_off = s_tot_slots + s_slots[tid] - ns;
+    if (b < p.num_rows) {
+      if (mixed) dec_base[b] = dec ? s_off : -1;
+      for (int k = 0; k < ns; ++k)
+        if (s_off + k < max_slots) slot_tok[s_off + k] = qs + k;
+      for (int m = 0; m < nt; ++m)
+        if (t_off + m < max_tiles) tiles[t_off + m] = make_int2(b, nt - 1 - m);
+    }
+    __syncthreads();
+    if (tid == 1023) {
+      s_tot_tiles += s_tiles[1023];
+      s_tot_slots += s_slots[1023];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    hdr->n_tiles = (uint32_t)min(s_tot_tiles, max_tiles);
+    hdr->n_slots = (uint32_t)min((int64_t)s_tot_slots, max_slots);
+  }
+}
+
+cudaError_t launch_plan(const AttnArgs& a, int mode_mixed, int max_decode_q, int bm,
+                        int max_tiles, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(a.p.err);
+  plan_kernel<<<1, 1024, 0, st>>>(a, mode_mixed, max_decode_q, bm, hdr,
+                                  const_cast<int32_t*>(a.dec_base),
+                                  const_cast<int32_t*>(a.slot_tok), const_cast<int2*>(a.tiles),
+                                  max_tiles, a.max_slots);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Merge (vllm-rlt PR #128, "Purpose", decode: the second kernel combining the
+// 16 fp32 partial states of a (row, head)).  For one decode token and query
+// head: M = max_k m_k over the splits with l_k > 0, w_k = 2^(m_k - M),
+// out = (sum_k w_k acc_k) / (sum_k w_k l_k) * v_scale, summed in the fixed
+// order k = 0..15 so a row's result never depends on the batch.  A token
+// with no visible key gets 0.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint32_t* n_slots_dev,
+                                                   int n_slots) {
+  const Problem& p = a.p;
+  const int slot = blockIdx.x;
+  const int h = blockIdx.y;
+  if (n_slots_dev && slot >= (int)*n_slots_dev) return;
+  if (slot >= n_slots) return;
+  const int t = a.slot_tok ? a.slot_tok[slot] : slot;
+  // row of token t: largest b with cu_q[b] <= t
+  int lo = 0, hi = p.num_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int L = __ldg(p.seq_lens + lo);
+  const int n_tiles = (L + DEC_KT - 1) / DEC_KT;
+  const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
+  const int nsp = tps ? (n_tiles + tps - 1) / tps : 0;
+
+  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * NSPLIT;
+  float mstar = -INFINITY;
+  for (int k = 0; k < nsp; ++k) {
+    const float2 v = ml[k];
+    if (v.y > 0.f) mstar = fmaxf(mstar, v.x);
+  }
+  float w[NSPLIT];
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k) {
+    w[k] = 0.f;
+    if (k < nsp) {
+      const float2 v = ml[k];
+      if (v.y > 0.f) {
+        w[k] = exp2f(v.x - mstar);
+        lsum += w[k] * v.y;
+      }
+    }
+  }
+  const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * NSPLIT * D;
+  T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
+  for (int c = threadIdx.x; c < D; c += 64) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NSPLIT; ++k)
+      if (w[k] != 0.f) s += w[k] * acc[k * D + c];
+    out[c] = from_float<T>(s * inv);
+  }
+}
+
+cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream_t st) {
+  if (n_slots <= 0 || a.p.num_rows == 0) return cudaSuccess;
+  const uint32_t* nsd =
+      a.slot_tok ? &reinterpret_cast<const WsHeader*>(a.p.err)->n_slots : nullptr;
+  dim3 grid(n_slots, a.p.hq);
+#define PA_M(TT, DD)                                                     \
+  if (a.p.d == DD) {                                                     \
+    merge_kernel<TT, DD><<<grid, 64, 0, st>>>(a, nsd, n_slots);          \
+    return cudaGetLastError();                                           \
+  }
+  if (q_dtype == PA_BF16) {
+    PA_M(__nv_bfloat16, 64) PA_M(__nv_bfloat16, 128) PA_M(__nv_bfloat16, 256)
+  } else if (q_dtype == PA_F16) {
+    PA_M(__half, 64) PA_M(__half, 128) PA_M(__half, 256)
+  } else if (q_dtype == PA_F32) {
+    PA_M(float, 64) PA_M(float, 128) PA_M(float, 256)
+  }
+#undef PA_M
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// fp32 path: full-precision fp32 products on the FMA pipes (vllm-rlt PR #128,
+// "Purpose", prefill bullets: fp32 inputs keep IEEE fp32 multiplies, with no
+// reduced-precision tensor-core arithmetic).  A CTA owns 16 GQA-packed query rows of
+// one (row, KV head) and either one decode split (partial state out, the same
+// partition and merge as the 16-bit path) or the row's whole causal range
+// (normalized output).  Warp w holds rows 4w..4w+3; each lane holds d/32
+// consecutive columns; keys are taken one at a time.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(128) f32_kernel(const AttnArgs a, int decode_mode) {
+  constexpr int E = D / 32;
+  const Problem& p = a.p;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int b, mblk, kh, split = 0;
+  if (decode_mode) {
+    b = blockIdx.x / a.dec_mblk;
+    mblk = blockIdx.x % a.dec_mblk;
+    kh = blockIdx.y / NSPLIT;
+    split = blockIdx.y % NSPLIT;
+  } else {
+    if (blockIdx.x >= *a.n_tiles) return;
+    const int2 t = a.tiles[blockIdx.x];
+    b = t.x;
+    mblk = t.y;
+    kh = blockIdx.y;
+  }
+  const int qs = p.cu_q[b];
+  const int qb = p.cu_q[b + 1] - qs;
+  const int L = p.seq_lens[b];
+  if (qb <= 0) return;
+  if (qs < 0 || qs + qb > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return;
+  }
+  int slot_base = qs;
+  if (decode_mode && a.dec_base) {
+    slot_base = a.dec_base[b];
+    if (slot_base < 0) return;
+  }
+  if (decode_mode && qb > a.max_decode_q && mblk == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    atomicOr(p.err, PA_DEVERR_DECODE_Q);
+  if (decode_mode && (int64_t)slot_base + qb > a.max_slots) return;
+  const int g = p.g, M = qb * g;
+  const int r0 = mblk * 16;
+  if (r0 >= M) return;
+  int k0, k1;
+  if (decode_mode) {
+    const int n_tiles = (L + DEC_KT - 1) / DEC_KT;
+    const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
+    k0 = split * tps * DEC_KT;
+    if (k0 >= L) return;
+    k1 = min(k0 + tps * DEC_KT, L);
+  } else {
+    k0 = 0;
+    k1 = min(L, L - qb + (min(r0 + 16, M) - 1) / g + 1);
+  }
+
+  const float* qp = static_cast<const float*>(a.q);
+  const float* kc = static_cast<const float*>(a.kc);
+  const float* vc = static_cast<const float*>(a.vc);
+  float qv[4][E], o[4][E], m[4], l[4];
+  int last[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int R = r0 + warp * 4 + r;
+    last[r] = R < M ? L - qb + R / g : -1;
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      o[r][e] = 0.f;
+      qv[r][e] = R < M ? qp[((int64_t)(qs + R / g) * p.hq + kh * g + R % g) * D + lane * E + e] : 0.f;
+    }
+  }
+  int kmax = k1 - 1;
+  kmax = min(kmax, max(max(last[0], last[1]), max(last[2], last[3])));
+  for (int j = k0; j <= kmax; ++j) {
+    const int64_t off = kv_offset(p, b, j, kh);
+    float kv[E], vv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      kv[e] = off >= 0 ? kc[off + lane * E + e] : 0.f;
+      vv[e] = off >= 0 ? vc[off + lane * E + e] : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) s = fmaf(qv[r][e], kv[e], s);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o2);
+      if (j > last[r]) continue;
+      const float x = s * p.sl2;
+      const float mn = fmaxf(m[r], x);
+      const float al = exp2f(m[r] - mn);
+      const float pj = exp2f(x - mn);
+      l[r] = l[r] * al + pj;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[r][e] = fmaf(pj, vv[e], o[r][e] * al);
+      m[r] = mn;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int R = r0 + warp * 4 + r;
+    if (R >= M) continue;
+    const int i = R / g, hg = R % g;
+    if (decode_mode) {
+      const int64_t slot = slot_base + i;
+      const int64_t base = (slot * p.hq + kh * g + hg) * NSPLIT + split;
+#pragma unroll
+      for (int e = 0; e < E; ++e) a.part_acc[base * D + lane * E + e] = o[r][e];
+      if (lane == 0) a.part_ml[base] = make_float2(m[r], l[r]);
+    } else {
+      const float inv = l[r] > 0.f ? p.v_scale / l[r] : 0.f;
+      float* out = static_cast<float*>(a.out) + ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
+#pragma unroll
+      for (int e = 0; e < E; ++e) out[lane * E + e] = o[r][e] * inv;
+    }
+  }
+}
+
+cudaError_t launch_f32(const AttnArgs& a, int decode_mode, int grid_x, int n_mblk,
+                       cudaStream_t st) {
+  dim3 grid;
+  if (decode_mode) {
+    if (a.p.num_rows == 0 || n_mblk == 0) return cudaSuccess;
+    grid = dim3((unsigned)a.p.num_rows * n_mblk, a.p.hkv * NSPLIT);
+  } else {
+    if (grid_x == 0) return cudaSuccess;
+    grid = dim3(grid_x, a.p.hkv);
+  }
+  switch (a.p.d) {
+    case 64: f32_kernel<64><<<grid, 128, 0, st>>>(a, decode_mode); break;
+    case 128: f32_kernel<128><<<grid, 128, 0, st>>>(a, decode_mode); break;
+    case 256: f32_kernel<256><<<grid, 128, 0, st>>>(a, decode_mode); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

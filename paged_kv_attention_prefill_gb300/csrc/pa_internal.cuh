@@ -1,0 +1,234 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "paged_attn.h"
+
+namespace pa {
+
+// Per-device "done once" flags (for function attributes, which are set per
+// device).  Racing threads may both run the action; it is idempotent.
+struct DeviceFlags {
+  std::atomic<uint64_t> mask{0};
+  template <typename F>
+  cudaError_t once(F&& f) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = f();
+    if (e == cudaSuccess) mask.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Workspace layout (offsets in bytes from the workspace start).
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t err;          // sticky PA_DEVERR_* flags
+  uint32_t n_tiles;      // prefill work items written by the plan kernel
+  uint32_t n_slots;      // decode token slots written by the plan kernel
+  uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct WsLayout {
+  size_t dec_base;   // int32 [num_rows]   partial-slot base of each decode row, -1 otherwise
+  size_t slot_tok;   // int32 [max_slots]  global token of each decode slot
+  size_t tiles;      // int2  [max_tiles]  (row, m-block) prefill work items
+  size_t part_acc;   // float [max_slots, Hq, NSPLIT, d]
+  size_t part_ml;    // float2[max_slots, Hq, NSPLIT]  (m in log2 units, l)
+  size_t total;
+  int64_t max_slots;
+  int64_t max_tiles;
+};
+
+constexpr int NSPLIT = 16;      // split-KV parts per decode row
+constexpr int DEC_KT = 64;      // keys per decode tile; the split partition unit
+constexpr int DEC_ROWS = 16;    // GQA-packed query rows per decode CTA
+constexpr int PF_BM = 64;       // GQA-packed query rows per prefill CTA (mma.sync path)
+
+WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g);
+
+// ---------------------------------------------------------------------------
+// Device-side problem description, passed by value to every kernel.
+// ---------------------------------------------------------------------------
+struct Problem {
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* bt;
+  int num_rows;
+  int total_q;     // rows of q / out: a row whose tokens fall outside is skipped
+  int max_pages;
+  int num_pages;
+  int page_size;
+  int hq, hkv, g, d;
+  float sl2;       // softmax_scale * k_scale * log2(e): logits in log2 units
+  float v_scale;
+  uint32_t* err;
+};
+
+struct AttnArgs {
+  Problem p;
+  const void* q;
+  const void* kc;
+  const void* vc;
+  void* out;
+  float* part_acc;
+  float2* part_ml;
+  const int32_t* dec_base;   // mixed: slot base per row (-1: not a decode row); null: slot = token
+  const int32_t* slot_tok;   // mixed: global token per slot; null: slot = token
+  const int2* tiles;         // prefill work list
+  const uint32_t* n_tiles;   // its length (device)
+  int max_decode_q;
+  int64_t max_slots;         // decode slots the workspace holds
+  int dec_mblk;              // decode grid: 16-row query blocks per row
+};
+
+// Launchers (one per translation unit family).  Return cudaError_t.
+cudaError_t launch_plan(const AttnArgs& a, int mode_mixed, int max_decode_q, int bm,
+                        int max_tiles, cudaStream_t st);
+cudaError_t launch_decode_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
+                              cudaStream_t st);
+cudaError_t launch_prefill_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int max_tiles,
+                               cudaStream_t st);
+cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream_t st);
+cudaError_t launch_f32(const AttnArgs& a, int decode_mode, int grid_x, int n_mblk,
+                       cudaStream_t st);
+bool prefill_mma_supported(int q_dtype, int kv_dtype, int d);
+bool decode_mma_supported(int q_dtype, int kv_dtype, int d);
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 zero-fills the chunk
+// (the source address is then not read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D, m16n8k16, fp32 accumulate.
+template <typename T>
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float* c, const uint32_t* a, uint32_t b0,
+                                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__half>(float* c, const uint32_t* a, uint32_t b0,
+                                                 uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> packed pair of 16-bit values (round to nearest even).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ __half from_float<__half>(float x) {
+  return __float2half_rn(x);
+}
+template <>
+__device__ __forceinline__ float from_float<float>(float x) {
+  return x;
+}
+
+// fp8 E5M2 has the sign, exponent and top two fraction bits of binary16, so
+// placing a code in the high byte of a 16-bit word gives the same value as a
+// binary16, exactly.  For a bf16 target the binary16 is widened to fp32 and
+// narrowed to bf16, also exactly (every E5M2 value is a bf16 value).
+template <typename T>
+__device__ __forceinline__ void e5m2x4_to(uint32_t w, uint32_t& lo, uint32_t& hi);
+template <>
+__device__ __forceinline__ void e5m2x4_to<__half>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(w, 0u, 0x1404);
+  hi = __byte_perm(w, 0u, 0x3424);
+}
+template <>
+__device__ __forceinline__ void e5m2x4_to<__nv_bfloat16>(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  uint32_t h0 = __byte_perm(w, 0u, 0x1404), h1 = __byte_perm(w, 0u, 0x3424);
+  __half2 a = *reinterpret_cast<__half2*>(&h0), b = *reinterpret_cast<__half2*>(&h1);
+  float2 fa = __half22float2(a), fb = __half22float2(b);
+  lo = pack2<__nv_bfloat16>(fa.x, fa.y);
+  hi = pack2<__nv_bfloat16>(fb.x, fb.y);
+}
+
+// Physical element offset of key j of row b, KV head kh, or -1 if the block
+// table entry is out of range (then the error flag is raised).
+__device__ __forceinline__ int64_t kv_offset(const Problem& p, int b, int j, int kh) {
+  const int P = p.page_size;
+  const int col = j / P;
+  if (col >= p.max_pages) {
+    atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return -1;
+  }
+  const int page = __ldg(p.bt + (int64_t)b * p.max_pages + col);
+  if (page < 0 || page >= p.num_pages) {
+    atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return -1;
+  }
+  return (((int64_t)page * P + (j % P)) * p.hkv + kh) * (int64_t)p.d;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace pa

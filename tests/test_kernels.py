@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Tolerances (max-abs error against the oracle): 1e-2 for bf16/fp16 inputs,
+2e-2 for an fp8 E5M2 KV cache, 1e-5 for fp32.  Invariants the pages state are
+checked bitwise: page size, physical-page order, a row alone vs in a batch,
+the mixed call vs the single-path calls, repeated calls; empty rows give
+exact zeros and poisoned (even NaN) cache slots outside the rows never leak.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_attention_prefill_gb300 as pa
+from paged_kv_attention_prefill_gb300 import build as pa_build
+from paged_kv_attention_prefill_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "f16": 1e-2, "f32": 1e-5, "e5m2": 2e-2}
+ENTRY = {"prefill": pa.paged_attn_prefill, "decode": pa.paged_attn_decode,
+         "mixed": pa.paged_attn_mixed}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pa_build.build()
+    oracle.build()
+    torch.cuda.init()
+
+
+def tol_of(b):
+    return TOL["e5m2"] if b.kv_dtype == "e5m2" else TOL[b.q_dtype]
+
+
+def run(entry, b, host=True, **kw):
+    """Runs one entry point on batch b (already on the GPU)."""
+    extra = {}
+    if host:
+        extra = dict(cu_seqlens_q_host=b.cu_seqlens_q.cpu(), seq_lens_host=b.seq_lens.cpu())
+    out = ENTRY[entry](b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens,
+                       softmax_scale=b.softmax_scale, k_scale=b.k_scale, v_scale=b.v_scale,
+                       **extra, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def ref_of(b, tokens=None):
+    return oracle.paged_attention(tokens=tokens, **b.oracle_args())
+
+
+def max_err(out, ref):
+    o = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(o).all(), "non-finite output"
+    return float(np.abs(o - ref).max()) if o.size else 0.0
+
+
+def small(q_lens, kv_lens, *, hq=8, hkv=2, d=128, P=16, dtype="bf16", kv_dtype=None, seed=0,
+          **kw):
+    b = workloads.make_batch(q_lens, kv_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             page_size=P, q_dtype=dtype, kv_dtype=kv_dtype, seed=seed, **kw)
+    return b, b.to("cuda")
+
+
+def assert_bitwise(a, b):
+    assert torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
+                       b.view(torch.uint8) if b.dtype != torch.uint8 else b)
+
+
+# --------------------------------------------------------------------------
+# small ragged cases, every path, every dtype / head dim
+# --------------------------------------------------------------------------
+
+PREFILL_LENS = ([65, 130, 1, 7, 200, 64], [65, 500, 1, 40, 1000, 64])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (6, 1), (4, 4)])
+def test_prefill_small(dtype, d, hq, hkv):
+    cpu, gpu = small(*PREFILL_LENS, hq=hq, hkv=hkv, d=d, P=32, dtype=dtype, seed=d + hq)
+    out = run("prefill", gpu)
+    assert max_err(out, ref_of(cpu)) <= TOL[dtype]
+
+
+DECODE_LENS = [0, 1, 31, 32, 33, 511, 512, 513, 4097, 10000]
+
+
+@pytest.mark.parametrize("dtype,kv", [("bf16", None), ("f16", None), ("f32", None),
+                                      ("f16", "e5m2"), ("bf16", "e5m2")])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_decode_small(dtype, kv, d):
+    ql = [1, 1, 1, 1, 4, 5, 1, 16, 4, 1]      # row 0: L = 0, an empty row
+    cpu, gpu = small(ql, DECODE_LENS, hq=8, hkv=2, d=d, P=16, dtype=dtype, kv_dtype=kv,
+                     seed=3 * d, k_scale=0.37 if kv else 1.0, v_scale=1.7 if kv else 1.0)
+    out = run("decode", gpu)
+    tol = TOL["e5m2"] if kv else TOL[dtype]
+    assert max_err(out, ref_of(cpu)) <= tol
+
+
+@pytest.mark.parametrize("dtype,kv", [("bf16", None), ("f16", "e5m2"), ("f32", None)])
+def test_mixed_small_and_routing_bitwise(dtype, kv):
+    ql = [300, 1, 4, 0, 17, 16, 2]
+    kl = [900, 700, 90, 0, 17, 2000, 2]
+    cpu, gpu = small(ql, kl, hq=12, hkv=2, d=128, P=48, dtype=dtype, kv_dtype=kv, seed=9)
+    out = run("mixed", gpu)
+    assert max_err(out, ref_of(cpu)) <= tol_of(cpu)
+    # rows routed to decode equal the decode call's rows; the others the prefill call's
+    cu = cpu.cu_seqlens_q.tolist()
+    dec_rows = [r for r, q in enumerate(ql) if 1 <= q <= 16]
+    pre_rows = [r for r, q in enumerate(ql) if q > 16]
+    for rows, entry in ((dec_rows, "decode"), (pre_rows, "prefill")):
+        sub_cpu = workloads.sub_batch(cpu, rows)
+        sub_out = run(entry, sub_cpu.to("cuda"))
+        got = torch.cat([out[cu[r]:cu[r + 1]] for r in rows])
+        assert_bitwise(got, sub_out)
+
+
+def test_mixed_without_host_mirrors_matches():
+    ql, kl = [100, 1, 3, 0], [400, 300, 50, 0]
+    cpu, gpu = small(ql, kl, seed=11)
+    a = run("mixed", gpu, host=True)
+    b = run("mixed", gpu, host=False)
+    assert_bitwise(a, b)
+    cpu2, gpu2 = small([1, 3, 2], [40, 50, 1000], seed=12)
+    assert_bitwise(run("decode", gpu2, host=True), run("decode", gpu2, host=False))
+    a = run("prefill", gpu, host=True)
+    b = run("prefill", gpu, host=False)
+    assert_bitwise(a, b)
+
+
+# --------------------------------------------------------------------------
+# invariants
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("entry", ["prefill", "mixed", "decode"])
+def test_page_size_and_permutation_invariance_bitwise(entry):
+    if entry == "decode":
+        ql, kl = [1, 4, 1, 5], [1, 700, 2049, 64]
+    else:
+        ql, kl = [70, 1, 129, 5], [70, 700, 2049, 64]
+    base = run(entry, small(ql, kl, P=16, seed=21)[1])
+    for P in (32, 64, 784, 816, 896):
+        assert_bitwise(run(entry, small(ql, kl, P=P, seed=21)[1]), base)
+    assert_bitwise(run(entry, small(ql, kl, P=16, seed=21, perm_seed=5)[1]), base)
+
+
+@pytest.mark.parametrize("entry", ["prefill", "mixed", "decode"])
+def test_row_alone_equals_row_in_batch(entry):
+    if entry == "decode":
+        ql, kl = [1, 4, 1, 5, 1], [1, 700, 2049, 64, 9000]
+    else:
+        ql, kl = [70, 1, 129, 5, 300], [70, 700, 2049, 64, 9000]
+    cpu, gpu = small(ql, kl, seed=22)
+    full = run(entry, gpu)
+    cu = cpu.cu_seqlens_q.tolist()
+    for r in range(len(ql)):
+        alone = run(entry, workloads.sub_batch(cpu, [r]).to("cuda"))
+        assert_bitwise(alone, full[cu[r]:cu[r + 1]])
+
+
+def test_empty_rows_zero_and_nan_poison_does_not_leak():
+    ql, kl = [1, 0, 1, 70, 1, 3], [0, 0, 33, 100, 17, 2]   # rows 0 and 5: tokens with no key
+    for entry in ("mixed", "prefill"):
+        cpu, gpu = small(ql, kl, seed=23, poison="nan")
+        out = run(entry, gpu)
+        assert torch.isfinite(out.float()).all()
+        assert (out[0] == 0).all()          # row 0 has L = 0
+        assert max_err(out, ref_of(cpu)) <= TOL["bf16"]
+    cpu, gpu = small([1, 1, 1], [0, 17, 0], seed=24, poison="nan", dtype="f16", kv_dtype="e5m2")
+    out = run("decode", gpu)
+    assert (out[0] == 0).all() and (out[2] == 0).all()
+    assert max_err(out, ref_of(cpu)) <= TOL["e5m2"]
+
+
+def test_repeated_calls_bitwise_and_no_device_errors():
+    cpu, gpu = small([100, 1, 4], [1000, 3000, 40], seed=25)
+    ws = pa.make_workspace(pa.make_params(gpu.q, gpu.k_cache), 3, gpu.total_q, "cuda")
+    a = run("mixed", gpu, workspace=ws)
+    b = run("mixed", gpu, workspace=ws)
+    assert_bitwise(a, b)
+    assert pa.read_errors(ws) == 0
+
+
+def test_device_flags_bad_block_table_entry_without_fault():
+    # the host mirrors are withheld so only the kernels can see the bad entry;
+    # the kernels must not dereference it and must raise the sticky flag
+    cpu, gpu = small([1, 20], [40, 60], seed=26)
+    bt = gpu.block_table.clone()
+    bt[0, 1] = 10 ** 6           # out of range
+    bt[1, 0] = -7                # negative
+    ws = pa.make_workspace(pa.make_params(gpu.q, gpu.k_cache), 2, gpu.total_q, "cuda")
+    for entry in ("mixed", "prefill"):
+        ENTRY[entry](gpu.q, gpu.k_cache, gpu.v_cache, bt, gpu.cu_seqlens_q, gpu.seq_lens,
+                     workspace=ws)
+        torch.cuda.synchronize()
+        assert pa.read_errors(ws) & 0x1
+    assert pa.read_errors(ws) == 0   # cleared by the read
+
+
+# --------------------------------------------------------------------------
+# the five workloads
+# --------------------------------------------------------------------------
+
+def test_workload1_decode_only():
+    cpu = workloads.make_workload(1)
+    gpu = cpu.to("cuda")
+    out = run("decode", gpu)
+    assert max_err(out, ref_of(cpu)) <= TOL["bf16"]
+    assert_bitwise(run("mixed", gpu), out)
+
+
+def _sample_tokens(cpu_q_lens, every=17, edge=32):
+    toks, base = [], 0
+    for q in cpu_q_lens:
+        idx = set(range(min(edge, q))) | set(range(max(0, q - edge), q)) | set(range(0, q, every))
+        toks += [base + i for i in sorted(idx)]
+        base += q
+    return toks
+
+
+def test_workload2_varlen_prefill_full_size():
+    outs = {}
+    for P in (16, 32, 64):
+        gpu = workloads.make_workload(2, device="cuda", data_device="cuda", page_size=P)
+        outs[P] = run("mixed", gpu)
+        if P == 16:
+            direct = run("prefill", gpu)
+            assert_bitwise(direct, outs[16])
+            ql = gpu.q_lens
+            toks = _sample_tokens(ql, every=97, edge=8)
+            cpu = gpu.to("cpu")
+            ref = ref_of(cpu, tokens=toks)
+            assert max_err(outs[16][toks], ref) <= TOL["bf16"]
+        del gpu
+        torch.cuda.empty_cache()
+    assert_bitwise(outs[32], outs[16])
+    assert_bitwise(outs[64], outs[16])
+
+
+def test_workload3_mixed_pages_784_816_896():
+    outs = {}
+    for P in (784, 816, 896):
+        gpu = workloads.make_workload(3, device="cuda", data_device="cuda", page_size=P)
+        outs[P] = run("mixed", gpu)
+        if P == 784:
+            # decode rows in full, the chunk's rows sampled
+            cpu_rows = workloads.sub_batch(gpu, [1, 2, 3])
+            out_rows = outs[P][2048:]
+            assert max_err(out_rows, ref_of(cpu_rows)) <= TOL["f16"]
+            cpu0 = workloads.sub_batch(gpu, [0])
+            toks = [0, 1, 2, 500, 1023, 1500, 2046, 2047]
+            assert max_err(outs[P][toks], ref_of(cpu0, tokens=toks)) <= TOL["f16"]
+        del gpu
+        torch.cuda.empty_cache()
+    assert_bitwise(outs[816], outs[784])
+    assert_bitwise(outs[896], outs[784])
+
+
+def test_workload4_split_kv_decode_batch_invariance():
+    gpu = workloads.make_workload(4, device="cuda", data_device="cuda")
+    out = run("decode", gpu)
+    assert_bitwise(run("mixed", gpu), out)
+    lens = gpu.kv_lens
+    rows = list(range(6)) + list(range(6, 256, 23))
+    cpu = workloads.sub_batch(gpu, rows)
+    ref = ref_of(cpu)
+    assert max_err(out[rows], ref) <= TOL["bf16"]
+    # every row alone equals the row in the batch, bitwise
+    for r in range(256):
+        alone = run("decode", workloads.sub_batch(gpu, [r], device="cuda"))
+        assert_bitwise(alone, out[r:r + 1])
+    assert all((out[r] == 0).all() for r in range(256) if lens[r] == 0)
+
+
+@pytest.mark.parametrize("scales", [(0.5, 2.0), (0.37, 1.7)])
+def test_workload5_long_context_fp8(scales):
+    gpu = workloads.make_workload(5, device="cuda", data_device="cuda", k_scale=scales[0],
+                                  v_scale=scales[1])
+    out = run("decode", gpu)
+    assert_bitwise(run("mixed", gpu), out)
+    ql = gpu.q_lens
+    cu = np.cumsum([0] + ql)
+    rows = [0, 1, 17, 40, 63]
+    cpu = workloads.sub_batch(gpu, rows)
+    ref = ref_of(cpu)
+    got = torch.cat([out[cu[r]:cu[r + 1]] for r in rows])
+    assert max_err(got, ref) <= TOL["e5m2"]
