@@ -384,6 +384,30 @@ def run_reference(args):
     return res
 
 
+def run_profile(args):
+    """Runs one part of the path `steps` times with no reporting: the command
+    that ncu captures.  --profile-rows keeps the first R rows of the
+    workload (a small case of the same kernel)."""
+    import paged_kv_attention_prefill_gb300 as pa
+    from paged_kv_attention_prefill_gb300 import build as pa_build
+    pa_build.build()
+    n = {"prefill": 2, "mixed3": 3, "decode4": 4, "decode5": 5, "decode1": 1}[args.profile]
+    full = workloads.make_workload(n, device="cuda", data_device="cuda")
+    b = full if not args.profile_rows else workloads.sub_batch(
+        full, list(range(min(args.profile_rows, full.num_rows))), device="cuda")
+    del full
+    torch.cuda.empty_cache()
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    fn = pa.paged_attn_decode if args.profile.startswith("decode") else pa.paged_attn_mixed
+    for _ in range(args.warmup + args.steps):
+        fn(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens, out=out,
+           workspace=ws, **call_args(b))
+    torch.cuda.synchronize()
+    print(f"profiled {args.profile}: rows={b.num_rows} total_q={b.total_q} "
+          f"cache={2 * b.k_cache.numel() * b.k_cache.element_size() / 2**20:.0f} MiB")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,7 +417,11 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
+    ap.add_argument("--profile", choices=["prefill", "mixed3", "decode4", "decode5", "decode1"])
+    ap.add_argument("--profile-rows", type=int, default=0)
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
