@@ -185,6 +185,8 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
 #define PA_DEVERR_BAD_PAGE   0x1u  /* a needed block-table entry outside [0, num_pages),
                                       or a key past the row's block-table columns */
 #define PA_DEVERR_DECODE_Q   0x4u  /* a decode-path row with q_b > max_decode_q */
+#define PA_DEVERR_TIMEOUT    0x8u  /* a bounded in-kernel wait ran out; that CTA's rows
+                                      are incomplete (never expected; reported, not hung) */
 
 /*
  * Copies the workspace header's error flags to *flags (host) and clears

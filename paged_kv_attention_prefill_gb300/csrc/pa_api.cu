@@ -44,6 +44,8 @@ struct Resolved {
   int host_max_q_dec; // mixed/decode: largest q_b among decode rows (host mirrors)
   int host_tiles;     // prefill work items (host mirrors), for the tile height in use
   int host_slots;     // decode slots (host mirrors)
+  bool tc;            // prefill on the tcgen05 kernel
+  int pf_bm;          // query rows per prefill work item
 };
 
 // 0 = not checked, 1 = sm_103, 2 = other
@@ -117,6 +119,8 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g);
   if (ws_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
+  r->tc = prefill_tc_supported(r->qd, r->kvd, r->d, (int64_t)bat->num_pages * r->P);
+  r->pf_bm = r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
   r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
   r->host_max_q_dec = 0;
   r->host_tiles = 0;
@@ -126,7 +130,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
     const int32_t* lens = bat->seq_lens_host;
     if (bat->num_rows > 0 && cu[0] != 0) return PA_ERR_INVALID_ARG;
     if (cu[bat->num_rows] != bat->total_q) return PA_ERR_INVALID_ARG;
-    const int bm = r->qd == PA_F32 ? 16 : PF_BM;
+    const int bm = r->pf_bm;
     for (int b = 0; b < bat->num_rows; ++b) {
       const int qb = cu[b + 1] - cu[b];
       const int L = lens[b];
@@ -202,6 +206,7 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
 
 cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, cudaStream_t st) {
   if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
+  if (r.tc) return launch_prefill_tc(a, r.qd, grid_tiles, st);
   return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
 }
 
@@ -228,7 +233,7 @@ pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, con
   if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
-  const int bm = r.qd == PA_F32 ? 16 : PF_BM;
+  const int bm = r.pf_bm;
   const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
   cudaError_t e = launch_plan(a, 0, 0, bm, max_tiles, st);
   if (e != cudaSuccess) return PA_ERR_CUDA;
@@ -265,7 +270,7 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   uint8_t* base = static_cast<uint8_t*>(workspace);
   a.dec_base = reinterpret_cast<const int32_t*>(base + w.dec_base);
   a.slot_tok = reinterpret_cast<const int32_t*>(base + w.slot_tok);
-  const int bm = r.qd == PA_F32 ? 16 : PF_BM;
+  const int bm = r.pf_bm;
   const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
   cudaError_t e = launch_plan(a, 1, r.max_dq, bm, max_tiles, st);
   if (e != cudaSuccess) return PA_ERR_CUDA;

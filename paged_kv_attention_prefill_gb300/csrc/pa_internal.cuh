@@ -104,6 +104,10 @@ cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream
 cudaError_t launch_f32(const AttnArgs& a, int decode_mode, int grid_x, int n_mblk,
                        cudaStream_t st);
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int d);
+// tcgen05 prefill (16-bit q with a same-type cache, cache < 2^31 tokens)
+constexpr int PF_BM_TC = 128;
+bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
+cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st);
 bool decode_mma_supported(int q_dtype, int kv_dtype, int d);
 
 // ---------------------------------------------------------------------------

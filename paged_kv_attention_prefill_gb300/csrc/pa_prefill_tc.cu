@@ -1,0 +1,513 @@
+// Varlen causal paged prefill on the tcgen05 tensor cores (sm_103a).
+//
+// Computes the same attention as every other path of the library (the
+// packed-varlen interface with one block table per row and bottom-right
+// causal alignment, GQA, online softmax over key tiles: vllm-rlt PR #128,
+// "Purpose", prefill bullets), restructured for Blackwell:
+//
+//  * A CTA owns 128 GQA-packed query rows of one (row, KV head) -- the
+//    query heads that share the KV head stacked into the tile's M dimension
+//    (1Cat-vLLM PR #1279, commit 1) -- so each K/V tile read from HBM serves
+//    all g heads of the group.
+//  * Warp 0 (producer) gathers K/V tiles one 16-token page slot at a time
+//    with TMA (3-D tensor maps over [tokens, Hkv, d], 128-byte swizzle)
+//    straight from the block table into a multi-stage shared-memory ring;
+//    the page size only changes which token coordinate a slot starts at
+//    (1Cat-vLLM PR #616, original description: any page size that is a
+//    multiple of 16).  The slot that holds the row's last key is copied by
+//    hand with the keys past the row's end zero-filled, so no stale or
+//    poisoned cache bytes ever reach the value product.
+//  * Warp 1, one elected thread, issues tcgen05.mma: S = Q K^T (M=128,
+//    N = key tile, K = d) into one of two TMEM buffers, and O += P V
+//    (N = d) into a TMEM accumulator.  Commits signal the other warps.
+//  * Warps 4-7 (one query row per TMEM lane) read S from TMEM, apply the
+//    causal mask, run the online softmax, write P (16-bit) into shared
+//    memory for the second MMA, rescale O in TMEM when the running maximum
+//    grows by more than 2^8 (otherwise the stale maximum is kept: the final
+//    O / l is unchanged), and finally normalise O and store the rows.
+//
+// Every wait is bounded (about two seconds); a CTA that runs out sets a
+// workspace flag, drains its own copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "pa_sm100.cuh"
+
+namespace pa {
+namespace {
+
+using namespace sm100;
+
+template <int D>
+struct TcCfg {
+  static constexpr int BM = 128;                    // query rows per CTA = TMEM lanes
+  static constexpr int BN = D == 256 ? 64 : 128;    // keys per tile
+  static constexpr int STAGES = D == 64 ? 3 : 2;    // K/V tiles in the ring
+  static constexpr int NCH = D / 64;                // 128-byte column chunks of d
+  static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
+  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one tile
+  static constexpr uint32_t P_BYTES = BM * BN * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+  static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = 2 * BN;         // S double buffer in [0, 2 BN)
+  // barrier indices
+  static constexpr int B_KVF = 0, B_KVE = STAGES, B_SF = 2 * STAGES, B_SE = B_SF + 2,
+                       B_PF = B_SE + 2, B_PV = B_PF + 1, B_Q = B_PV + 1, B_DRAIN = B_Q + 1,
+                       NBAR = B_DRAIN + 1;
+  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NBAR * 8 <= 128, "barrier area");
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Bounded wait that ignores the abort flag: used to drain work this thread
+// itself started before its resources go away.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      atomicOr(err, PA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&x)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, float (&x)[128]) {
+  uint32_t r[128];
+  tmem_ld_x128(taddr, r);
+#pragma unroll
+  for (int k = 0; k < 128; ++k) x[k] = __uint_as_float(r[k]);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, float (&x)[64]) {
+  uint32_t r[64];
+  tmem_ld_x64(taddr, r);
+#pragma unroll
+  for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(r[k]);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256, 1)
+    prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using C = TcCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V,
+                 sP = base + C::OFF_P;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 132);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+  const Problem& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item (uniform over the CTA) -----------------------------------
+  if (blockIdx.x >= *a.n_tiles) return;
+  const int2 wi = a.tiles[blockIdx.x];
+  const int b = wi.x, mb = wi.y, kh = blockIdx.y;
+  const int qs = __ldg(p.cu_q + b);
+  const int qb = __ldg(p.cu_q + b + 1) - qs;
+  const int L = __ldg(p.seq_lens + b);
+  if (qb <= 0) return;
+  if (qs < 0 || qs + qb > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return;
+  }
+  const int g = p.g, M = qb * g, R0 = mb * C::BM;
+  if (R0 >= M) return;
+  const int r_last = min(R0 + C::BM, M) - 1;
+  const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
+  const int n_tiles = k_end > 0 ? (k_end + C::BN - 1) / C::BN : 0;
+
+  // ---- barriers and TMEM ----------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(C::B_KVF + s), 1);
+      mbar_init(bar(C::B_KVE + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_SF + s), 1);
+      mbar_init(bar(C::B_SE + s), 128);
+    }
+    mbar_init(bar(C::B_PF), 128);
+    mbar_init(bar(C::B_PV), 1);
+    mbar_init(bar(C::B_Q), 128);
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ======================= producer: K/V page slots ======================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int P = p.page_size;
+    const int64_t bt_row = (int64_t)b * p.max_pages;
+    int j = 0;
+    bool ok = true;
+    for (; j < n_tiles; ++j) {
+      const int st = j % C::STAGES;
+      if (j >= C::STAGES)
+        ok = mbar_wait(bar(C::B_KVE + st), ((j / C::STAGES) - 1) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const int kbase = j * C::BN;
+      const uint32_t dK = sK + st * C::KV_BYTES, dV = sV + st * C::KV_BYTES;
+      // slot `lane`: 1 = whole slot by TMA, 2 = partial (copy by hand), 3 = zero-fill
+      int kind = 0, tok0 = 0;
+      if (lane < C::SLOTS) {
+        const int s0 = kbase + 16 * lane;
+        if (s0 >= L) {
+          kind = 3;
+        } else {
+          const int col = s0 / P;
+          const int page = col < p.max_pages ? __ldg(p.bt + bt_row + col) : -1;
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+            kind = 3;
+          } else {
+            tok0 = page * P + (s0 % P);
+            kind = (s0 + 16 <= L) ? 1 : 2;
+          }
+        }
+      }
+      uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
+      while (manual) {
+        const int s = __ffs(manual) - 1;
+        manual &= manual - 1;
+        const int ks = __shfl_sync(0xffffffffu, kind, s);
+        const int t0 = __shfl_sync(0xffffffffu, tok0, s);
+        const int nvalid = ks == 2 ? L - (kbase + 16 * s) : 0;
+        for (int it = lane; it < 16 * C::NCH * 8 * 2; it += 32) {
+          const int kv = it & 1, piece = (it >> 1) & 7, rest = it >> 4;
+          const int c = rest % C::NCH, rr = rest / C::NCH;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (rr < nvalid) {
+            const T* src = static_cast<const T*>(kv ? a.vc : a.kc) +
+                           ((int64_t)(t0 + rr) * p.hkv + kh) * D + c * 64 + piece * 8;
+            v = __ldg(reinterpret_cast<const uint4*>(src));
+          }
+          const int row = 16 * s + rr;
+          st_shared_v4((kv ? dV : dK) + c * (C::BN * 128) + row * 128 + ((piece ^ (row & 7)) << 4),
+                       v);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
+      if (lane == 0) mbar_arrive_expect_tx(bar(C::B_KVF + st), (uint32_t)n_tma * 16u * D * 2u * 2u);
+      __syncwarp();
+      if (kind == 1) {
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c) {
+          const uint32_t off = c * (C::BN * 128) + lane * 16 * 128;
+          tma_load_3d(dK + off, &tmK, c * 64, kh, tok0, bar(C::B_KVF + st));
+          tma_load_3d(dV + off, &tmV, c * 64, kh, tok0, bar(C::B_KVF + st));
+        }
+      }
+    }
+    if (!ok) {
+      // copies this warp started may still be landing: wait for them
+      for (int jj = max(0, j - C::STAGES); jj < j; ++jj)
+        mbar_drain(bar(C::B_KVF + jj % C::STAGES), (jj / C::STAGES) & 1, p.err);
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (one thread) =======================
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+      constexpr uint32_t idS = idesc_f16(fmt, 128, C::BN, false);
+      constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
+      bool ok = n_tiles == 0 || mbar_wait(bar(C::B_Q), 0, abort_flag, p.err);
+      if (ok) tc_fence_after();
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          const int st = j % C::STAGES;
+          ok = mbar_wait(bar(C::B_KVF + st), (j / C::STAGES) & 1, abort_flag, p.err);
+          const int buf = j & 1;
+          if (ok && j >= 2) ok = mbar_wait(bar(C::B_SE + buf), ((j >> 1) - 1) & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dS = tmem + buf * C::BN;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(sQ + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(
+                sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+            tc_mma_f16(dS, ad, bd, idS, k > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_SF + buf));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, stp = jj % C::STAGES;
+          ok = mbar_wait(bar(C::B_PF), jj & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(sP + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t bd =
+                sdesc_sw128(sV + stp * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
+            tc_mma_f16(tmem + C::O_COL, ad, bd, idO, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_PV));
+          tc_commit(bar(C::B_KVE + stp));
+        }
+      }
+      // nothing this thread issued may still run once TMEM is freed
+      tc_commit(bar(C::B_DRAIN));
+      mbar_drain(bar(C::B_DRAIN), 0, p.err);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============ softmax / correction / epilogue: one row per thread =======
+    const int q4 = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q4 * 32 + lane;     // tile row == TMEM lane
+    const int R = R0 + r;
+    const bool valid = R < M;
+    const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
+    const int last = valid ? L - qb + i : -1;  // last visible key of this row
+    const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
+    {
+      const T* qrow = static_cast<const T*>(a.q) + qoff;
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) {
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc) {
+          const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + pc * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(sQ + c * (C::BM * 128) + r * 128 + ((pc ^ (r & 7)) << 4), v);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_Q));
+    }
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    const float sl2 = p.sl2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int buf = j & 1;
+      ok = mbar_wait(bar(C::B_SF + buf), (j >> 1) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[C::BN];
+      tmem_ld_row<C::BN>(trow + buf * C::BN, x);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_SE + buf));
+
+      const int kb = j * C::BN;
+      float mt = -INFINITY;
+      if (kb + C::BN - 1 <= last) {
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k) {
+          x[k] *= sl2;
+          mt = fmaxf(mt, x[k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k) {
+          x[k] = (kb + k <= last) ? x[k] * sl2 : -INFINITY;
+          mt = fmaxf(mt, x[k]);
+        }
+      }
+      const float m_new = fmaxf(m_used, mt);
+      float factor = 1.f;
+      bool need = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + 8.f) {
+        need = true;
+        factor = exp2f(m_used - m_new);
+        m_used = m_new;
+      }
+      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      float rs = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::BN; ++k) {
+        x[k] = exp2f(x[k] - mu);
+        rs += x[k];
+      }
+      // the previous tile's P V must be done: O is stable and P's buffer free
+      if (j >= 1) {
+        ok = mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::O_COL + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tmem_st_x32(trow + C::O_COL + c * 32, o);
+        }
+      }
+      l = l * factor + rs;
+#pragma unroll
+      for (int pc = 0; pc < C::BN / 8; ++pc) {
+        uint4 v;
+        v.x = pack2<T>(x[8 * pc + 0], x[8 * pc + 1]);
+        v.y = pack2<T>(x[8 * pc + 2], x[8 * pc + 3]);
+        v.z = pack2<T>(x[8 * pc + 4], x[8 * pc + 5]);
+        v.w = pack2<T>(x[8 * pc + 6], x[8 * pc + 7]);
+        const int c = pc >> 3, piece = pc & 7;
+        st_shared_v4(sP + c * (C::BM * 128) + r * 128 + ((piece ^ (r & 7)) << 4), v);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PF));
+    }
+    // ---- epilogue: out = O / l * v_scale ----
+    T* orow = static_cast<T*>(a.out) + qoff;
+    if (ok && n_tiles > 0) {
+      ok = mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const float inv = l > 0.f ? p.v_scale / l : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::O_COL + c * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 v;
+              v.x = pack2<T>(__uint_as_float(o[8 * w + 0]) * inv, __uint_as_float(o[8 * w + 1]) * inv);
+              v.y = pack2<T>(__uint_as_float(o[8 * w + 2]) * inv, __uint_as_float(o[8 * w + 3]) * inv);
+              v.z = pack2<T>(__uint_as_float(o[8 * w + 4]) * inv, __uint_as_float(o[8 * w + 5]) * inv);
+              v.w = pack2<T>(__uint_as_float(o[8 * w + 6]) * inv, __uint_as_float(o[8 * w + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + c * 32 + 8 * w) = v;
+            }
+          }
+        }
+      }
+    } else if (ok && valid) {
+      // no key visible to any row of the tile
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 64 elements.
+bool encode_kv_map(CUtensorMap* tm, const void* cache, int q_dtype, int d, int hkv,
+                   int64_t tokens) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
+  cuuint32_t box[3] = {64, 1, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      q_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(tm, dt, 3, const_cast<void*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D>
+cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
+                      cudaStream_t st) {
+  using C = TcCfg<D>;
+  auto k = prefill_tc_kernel<T, D>;
+  static DeviceFlags attr;
+  cudaError_t e = attr.once([&] {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (e != cudaSuccess) return e;
+  k<<<dim3(grid_x, a.p.hkv), 256, C::SMEM, st>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
+  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype &&
+         (d == 64 || d == 128 || d == 256) && cache_tokens < (int64_t(1) << 31) &&
+         encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st) {
+  if (grid_x == 0) return cudaSuccess;
+  const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
+  CUtensorMap tk, tv;
+  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+    return cudaErrorInvalidValue;
+  const bool bf = q_dtype == PA_BF16;
+  switch (a.p.d) {
+    case 64: return bf ? launch_tc<__nv_bfloat16, 64>(a, tk, tv, grid_x, st)
+                       : launch_tc<__half, 64>(a, tk, tv, grid_x, st);
+    case 128: return bf ? launch_tc<__nv_bfloat16, 128>(a, tk, tv, grid_x, st)
+                        : launch_tc<__half, 128>(a, tk, tv, grid_x, st);
+    case 256: return bf ? launch_tc<__nv_bfloat16, 256>(a, tk, tv, grid_x, st)
+                        : launch_tc<__half, 256>(a, tk, tv, grid_x, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa
