@@ -44,7 +44,10 @@ template <int D>
 struct TcCfg {
   static constexpr int BM = 128;                    // query rows per CTA = TMEM lanes
   static constexpr int BN = D == 256 ? 64 : 128;    // keys per tile
-  static constexpr int STAGES = D == 64 ? 3 : 2;    // K/V tiles in the ring
+  // K is released as soon as S = Q K^T is done, V only after O += P V, so
+  // the K ring runs further ahead than the V ring.
+  static constexpr int KS = D == 64 ? 4 : (D == 128 ? 3 : 2);
+  static constexpr int VS = D == 64 ? 3 : 2;
   static constexpr int NCH = D / 64;                // 128-byte column chunks of d
   static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
   static constexpr uint32_t Q_BYTES = BM * D * 2;
@@ -52,20 +55,27 @@ struct TcCfg {
   static constexpr uint32_t P_BYTES = BM * BN * 2;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
+  static constexpr uint32_t OFF_P = OFF_V + VS * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
   static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 2 * BN;         // S double buffer in [0, 2 BN)
   // barrier indices
-  static constexpr int B_KVF = 0, B_KVE = STAGES, B_SF = 2 * STAGES, B_SE = B_SF + 2,
-                       B_PF = B_SE + 2, B_PV = B_PF + 1, B_Q = B_PV + 1, B_DRAIN = B_Q + 1,
-                       NBAR = B_DRAIN + 1;
+  static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
+                       B_SF = 2 * KS + 2 * VS, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PV = B_PF + 1,
+                       B_Q = B_PV + 1, B_DRAIN = B_Q + 1, NBAR = B_DRAIN + 1;
   static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NBAR * 8 <= 128, "barrier area");
+  static_assert(NBAR * 8 <= 192, "barrier area");
 };
+
+// 2^x on the MUFU unit (approximate, flushes subnormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -114,8 +124,8 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V,
                  sP = base + C::OFF_P;
   const uint32_t bar0 = base + C::OFF_BAR;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 132);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 196);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   const Problem& p = a.p;
@@ -141,9 +151,13 @@ __global__ void __launch_bounds__(256, 1)
 
   // ---- barriers and TMEM ----------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar(C::B_KVF + s), 1);
-      mbar_init(bar(C::B_KVE + s), 1);
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(bar(C::B_KF + s), 1);
+      mbar_init(bar(C::B_KE + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      mbar_init(bar(C::B_VF + s), 1);
+      mbar_init(bar(C::B_VE + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SF + s), 1);
@@ -165,27 +179,29 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ======================= producer: K/V page slots ======================
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
+  if (warp == 0 || warp == 2) {
+    // ============== producers: warp 0 streams K tiles, warp 2 V tiles ========
+    const bool isK = warp == 0;
+    const int NS = isK ? C::KS : C::VS;
+    const int B_FULL = isK ? C::B_KF : C::B_VF, B_EMPTY = isK ? C::B_KE : C::B_VE;
+    const uint32_t ring = isK ? sK : sV;
+    const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+    const T* cache = static_cast<const T*>(isK ? a.kc : a.vc);
+    if (lane == 0) tma_prefetch_desc(tmap);
     const int P = p.page_size;
     const int64_t bt_row = (int64_t)b * p.max_pages;
     int j = 0;
     bool ok = true;
     for (; j < n_tiles; ++j) {
-      const int st = j % C::STAGES;
-      if (j >= C::STAGES)
-        ok = mbar_wait(bar(C::B_KVE + st), ((j / C::STAGES) - 1) & 1, abort_flag, p.err);
+      const int st = j % NS;
+      if (j >= NS) ok = mbar_wait(bar(B_EMPTY + st), ((j / NS) - 1) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       const int kbase = j * C::BN;
-      const uint32_t dK = sK + st * C::KV_BYTES, dV = sV + st * C::KV_BYTES;
-      // slot `lane`: 1 = whole slot by TMA, 2 = partial (copy by hand), 3 = zero-fill
+      const uint32_t dst = ring + st * C::KV_BYTES;
+      // slot `lane`: 1 = whole slot by TMA, 2 = partial (copied by hand), 3 = zero-fill
       int kind = 0, tok0 = 0;
       if (lane < C::SLOTS) {
         const int s0 = kbase + 16 * lane;
@@ -210,38 +226,34 @@ __global__ void __launch_bounds__(256, 1)
         const int ks = __shfl_sync(0xffffffffu, kind, s);
         const int t0 = __shfl_sync(0xffffffffu, tok0, s);
         const int nvalid = ks == 2 ? L - (kbase + 16 * s) : 0;
-        for (int it = lane; it < 16 * C::NCH * 8 * 2; it += 32) {
-          const int kv = it & 1, piece = (it >> 1) & 7, rest = it >> 4;
+        for (int it = lane; it < 16 * C::NCH * 8; it += 32) {
+          const int piece = it & 7, rest = it >> 3;
           const int c = rest % C::NCH, rr = rest / C::NCH;
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (rr < nvalid) {
-            const T* src = static_cast<const T*>(kv ? a.vc : a.kc) +
-                           ((int64_t)(t0 + rr) * p.hkv + kh) * D + c * 64 + piece * 8;
+            const T* src = cache + ((int64_t)(t0 + rr) * p.hkv + kh) * D + c * 64 + piece * 8;
             v = __ldg(reinterpret_cast<const uint4*>(src));
           }
           const int row = 16 * s + rr;
-          st_shared_v4((kv ? dV : dK) + c * (C::BN * 128) + row * 128 + ((piece ^ (row & 7)) << 4),
-                       v);
+          st_shared_v4(dst + c * (C::BN * 128) + row * 128 + ((piece ^ (row & 7)) << 4), v);
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
       const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
-      if (lane == 0) mbar_arrive_expect_tx(bar(C::B_KVF + st), (uint32_t)n_tma * 16u * D * 2u * 2u);
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + st), (uint32_t)n_tma * 16u * D * 2u);
       __syncwarp();
       if (kind == 1) {
 #pragma unroll
-        for (int c = 0; c < C::NCH; ++c) {
-          const uint32_t off = c * (C::BN * 128) + lane * 16 * 128;
-          tma_load_3d(dK + off, &tmK, c * 64, kh, tok0, bar(C::B_KVF + st));
-          tma_load_3d(dV + off, &tmV, c * 64, kh, tok0, bar(C::B_KVF + st));
-        }
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(dst + c * (C::BN * 128) + lane * 16 * 128, tmap, c * 64, kh, tok0,
+                      bar(B_FULL + st));
       }
     }
     if (!ok) {
       // copies this warp started may still be landing: wait for them
-      for (int jj = max(0, j - C::STAGES); jj < j; ++jj)
-        mbar_drain(bar(C::B_KVF + jj % C::STAGES), (jj / C::STAGES) & 1, p.err);
+      for (int jj = max(0, j - NS); jj < j; ++jj)
+        mbar_drain(bar(B_FULL + jj % NS), (jj / NS) & 1, p.err);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer (one thread) =======================
@@ -253,8 +265,8 @@ __global__ void __launch_bounds__(256, 1)
       if (ok) tc_fence_after();
       for (int j = 0; ok && j <= n_tiles; ++j) {
         if (j < n_tiles) {
-          const int st = j % C::STAGES;
-          ok = mbar_wait(bar(C::B_KVF + st), (j / C::STAGES) & 1, abort_flag, p.err);
+          const int st = j % C::KS;
+          ok = mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err);
           const int buf = j & 1;
           if (ok && j >= 2) ok = mbar_wait(bar(C::B_SE + buf), ((j >> 1) - 1) & 1, abort_flag, p.err);
           if (!ok) break;
@@ -268,10 +280,12 @@ __global__ void __launch_bounds__(256, 1)
             tc_mma_f16(dS, ad, bd, idS, k > 0 ? 1u : 0u);
           }
           tc_commit(bar(C::B_SF + buf));
+          tc_commit(bar(C::B_KE + st));
         }
         if (j >= 1) {
-          const int jj = j - 1, stp = jj % C::STAGES;
-          ok = mbar_wait(bar(C::B_PF), jj & 1, abort_flag, p.err);
+          const int jj = j - 1, stp = jj % C::VS;
+          ok = mbar_wait(bar(C::B_VF + stp), (jj / C::VS) & 1, abort_flag, p.err);
+          if (ok) ok = mbar_wait(bar(C::B_PF), jj & 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -282,7 +296,7 @@ __global__ void __launch_bounds__(256, 1)
             tc_mma_f16(tmem + C::O_COL, ad, bd, idO, (jj > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(bar(C::B_PV));
-          tc_commit(bar(C::B_KVE + stp));
+          tc_commit(bar(C::B_VE + stp));
         }
       }
       // nothing this thread issued may still run once TMEM is freed
@@ -331,35 +345,29 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive(bar(C::B_SE + buf));
 
       const int kb = j * C::BN;
-      float mt = -INFINITY;
-      if (kb + C::BN - 1 <= last) {
+      float mt = -INFINITY;  // max raw logit of the tile (masked keys -> -inf)
+      if (kb + C::BN - 1 > last) {
 #pragma unroll
-        for (int k = 0; k < C::BN; ++k) {
-          x[k] *= sl2;
-          mt = fmaxf(mt, x[k]);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < C::BN; ++k) {
-          x[k] = (kb + k <= last) ? x[k] * sl2 : -INFINITY;
-          mt = fmaxf(mt, x[k]);
-        }
+        for (int k = 0; k < C::BN; ++k)
+          if (kb + k > last) x[k] = -INFINITY;
       }
-      const float m_new = fmaxf(m_used, mt);
+#pragma unroll
+      for (int k = 0; k < C::BN; ++k) mt = fmaxf(mt, x[k]);
+      const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
       float factor = 1.f;
       bool need = false;
       if (j == 0) {
         m_used = m_new;
       } else if (m_new > m_used + 8.f) {
         need = true;
-        factor = exp2f(m_used - m_new);
+        factor = ex2(m_used - m_new);
         m_used = m_new;
       }
-      const float mu = m_used == -INFINITY ? 0.f : m_used;
+      const float nmu = m_used == -INFINITY ? 0.f : -m_used;
       float rs = 0.f;
 #pragma unroll
       for (int k = 0; k < C::BN; ++k) {
-        x[k] = exp2f(x[k] - mu);
+        x[k] = ex2(fmaf(x[k], sl2, nmu));
         rs += x[k];
       }
       // the previous tile's P V must be done: O is stable and P's buffer free
