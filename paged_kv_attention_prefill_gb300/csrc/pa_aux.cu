@@ -70,6 +70,54 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
     hdr->n_tiles = (uint32_t)min(s_tot_tiles, max_tiles);
     hdr->n_slots = (uint32_t)min((int64_t)s_tot_slots, max_slots);
   }
+
+  // Longest-first order of the prefill work items (by the keys the item's
+  // rows can see), so the CTAs dispatched last are the short ones.  Items
+  // are independent, so the order changes no result.  Lists longer than
+  // 4096 items keep row order.
+  __syncthreads();
+  const int n = min(s_tot_tiles, max_tiles);
+  if (n < 2 || n > 4096) return;
+  __shared__ unsigned long long keys[4096];
+  __shared__ int s_bad;
+  int npow = 2;
+  while (npow < n) npow <<= 1;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = tid; i < npow; i += 1024) {
+    unsigned long long key = 0ull;
+    if (i < n) {
+      const int2 t = tiles[i];
+      const int qs = p.cu_q[t.x], qb = p.cu_q[t.x + 1] - qs, L = p.seq_lens[t.x];
+      const int r_last = min((t.y + 1) * bm, qb * p.g) - 1;
+      const int work = max(0, min(L, L - qb + r_last / p.g + 1));
+      if (t.x >= (1 << 20) || t.y >= (1 << 12)) s_bad = 1;
+      key = ((unsigned long long)(unsigned)work << 32) | ((unsigned)t.x << 12) | (unsigned)t.y;
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  if (s_bad) return;
+  for (int k = 2; k <= npow; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < npow; i += 1024) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            keys[i] = y;
+            keys[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = tid; i < n; i += 1024) {
+    const unsigned long long key = keys[i];
+    tiles[i] = make_int2((int)((key >> 12) & 0xFFFFFu), (int)(key & 0xFFFu));
+  }
 }
 
 cudaError_t launch_plan(const AttnArgs& a, int mode_mixed, int max_decode_q, int bm,

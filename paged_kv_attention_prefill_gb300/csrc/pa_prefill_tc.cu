@@ -132,9 +132,11 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item (uniform over the CTA) -----------------------------------
-  if (blockIdx.x >= *a.n_tiles) return;
-  const int2 wi = a.tiles[blockIdx.x];
-  const int b = wi.x, mb = wi.y, kh = blockIdx.y;
+  // 1-D grid, KV head fastest: the (longest-first) work list is dispatched in order
+  const int item = blockIdx.x / p.hkv, kh = blockIdx.x % p.hkv;
+  if (item >= (int)*a.n_tiles) return;
+  const int2 wi = a.tiles[item];
+  const int b = wi.x, mb = wi.y;
   const int qs = __ldg(p.cu_q + b);
   const int qb = __ldg(p.cu_q + b + 1) - qs;
   const int L = __ldg(p.seq_lens + b);
@@ -487,7 +489,7 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMa
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3(grid_x, a.p.hkv), 256, C::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 256, C::SMEM, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
