@@ -83,18 +83,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Bounded wait that ignores the abort flag: used to drain work this thread
-// itself started before its resources go away.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint32_t* err) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-      atomicOr(err, PA_DEVERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
 template <int N>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&x)[N]);
 template <>
@@ -463,6 +451,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 64 elements.
 bool encode_kv_map(CUtensorMap* tm, const void* cache, int q_dtype, int d, int hkv,
                    int64_t tokens) {
@@ -478,6 +468,8 @@ bool encode_kv_map(CUtensorMap* tm, const void* cache, int q_dtype, int d, int h
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <typename T, int D>
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,

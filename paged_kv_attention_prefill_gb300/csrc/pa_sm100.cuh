@@ -65,6 +65,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that ignores the abort flag: used to drain work the calling
+// thread itself started (copies, MMAs) before its resources go away.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      atomicOr(err, PA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // async-proxy fences and TMA
 // ---------------------------------------------------------------------------
