@@ -199,7 +199,7 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
   if (r.qd == PA_F32)
     e = launch_f32(a, 1, 0, n_mblk, st);
   else if (decode_tma_supported(r.qd, r.kvd, r.d, (int64_t)a.p.num_pages * a.p.page_size))
-    e = launch_decode_tma(a, r.qd, n_mblk, st);
+    e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, st);
   else
     e = launch_decode_mma(a, r.qd, r.kvd, n_mblk, st);
   if (e != cudaSuccess) return e;

@@ -1,5 +1,4 @@
-// Split-KV paged decode for 16-bit KV caches: persistent warps, each with its
-// own TMA ring.
+// Split-KV paged decode: persistent warps, each with its own TMA ring.
 //
 // Same partition and partial states as the rest of the library (vllm-rlt PR
 // #128, "Purpose", decode bullets: each row's keys cut into NSPLIT
@@ -10,13 +9,22 @@
 //  * A work item is (row, KV head, split, 16-row block of GQA-packed query
 //    rows).  Each warp takes one item at a time from a counter in the
 //    workspace and streams the item's keys in 16-token page slots: one TMA
-//    box per 64 columns of K and of V, straight from the block table into
-//    the warp's private ring of NS slots.  The warp keeps NS-1 slots in
-//    flight and prefetches across item boundaries, so HBM never waits for a
-//    warp to start its next item.
+//    box per 128 bytes of a key row, for K and for V, straight from the
+//    block table into the warp's private ring of NS slots.  The warp keeps
+//    NS-1 slots in flight and prefetches across item boundaries, so HBM
+//    never waits for a warp to start its next item.
 //  * The math per slot is warp-level MMA (m16n8k16): S = Q K^T for the 16
 //    rows x 16 keys, the online softmax in registers, O += P V.  At the end
 //    of an item the warp writes (acc[d], m, l) of its rows for that split.
+//  * fp8 E5M2 caches (1Cat-vLLM PR #616, original description: an fp8_e5m2
+//    KV cache dequantized in the kernel): an E5M2 code in the high byte of a
+//    16-bit word is the same binary16 value, so K is widened straight from
+//    the raw slot into MMA operands -- four consecutive codes of one key
+//    become two fp16 pairs, and Q's reduction index is permuted the same way
+//    so the dot product is unchanged -- while V is widened once per slot
+//    into a 16-bit staging tile for the transposed fragment loads.  The
+//    per-tensor k_scale is folded into the logit scale, v_scale into the
+//    merge.
 //  * No block-wide barrier anywhere: warps only wait on their own mbarriers.
 //    All waits are clock-bounded.
 //
@@ -27,7 +35,7 @@
 #include "pa_sm100.cuh"
 
 namespace pa {
-bool encode_kv_map(CUtensorMap* tm, const void* cache, int q_dtype, int d, int hkv,
+bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
                    int64_t tokens);
 
 namespace {
@@ -36,26 +44,60 @@ using namespace sm100;
 
 constexpr int DEC_WARPS = 4;
 
-template <int D>
+template <int D, bool KV8>
 struct DecCfg {
-  static constexpr int NCH = D / 64;                      // 128-byte column chunks
-  static constexpr uint32_t HALF = 16 * D * 2;             // K (or V) of one 16-key slot
+  static constexpr int ELT = KV8 ? 1 : 2;
+  static constexpr int NCH = D * ELT / 128;                // 128-byte boxes per key row
+  static constexpr uint32_t HALF = 16 * D * ELT;           // K (or V) of one 16-key slot
   static constexpr uint32_t SLOT = 2 * HALF;
-  static constexpr uint32_t QB = 16 * D * 2;               // the item's 16 query rows
-  static constexpr int NS = D == 256 ? 3 : (D == 128 ? 6 : 8);  // ring slots per warp
-  static constexpr uint32_t WARP_BYTES = NS * SLOT + QB;   // multiple of 1024
-  static constexpr uint32_t OFF_BAR = DEC_WARPS * WARP_BYTES;
+  static constexpr int NS = KV8 ? (D == 256 ? 5 : 8) : (D == 256 ? 3 : (D == 128 ? 6 : 8));
+  static constexpr uint32_t STG = KV8 ? 16 * D * 2 : 0;    // widened V of one slot
+  static constexpr uint32_t QROW = KV8 ? D * 2 + 16 : D * 2;  // fp8: padded, unswizzled rows
+  static constexpr uint32_t QB = 16 * QROW;
+  static constexpr uint32_t AUX = STG + QB;
+  static constexpr uint32_t OFF_AUX = DEC_WARPS * NS * SLOT;  // all rings first (1 KB aligned)
+  static constexpr uint32_t OFF_BAR = OFF_AUX + DEC_WARPS * AUX;
   static constexpr uint32_t OFF_META = OFF_BAR + DEC_WARPS * NS * 8;
   static constexpr uint32_t SMEM = OFF_META + DEC_WARPS * NS * 8 + 1024;
-  static_assert(WARP_BYTES % 1024 == 0, "slot alignment");
+  static_assert(SLOT % 1024 == 0, "slot alignment");
+  static_assert(AUX % 16 == 0, "aux alignment");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ uint32_t swz_chunked(int row, int col_elem) {
-  // 16-bit element column -> byte offset in a [NCH][16 rows][128 B] tile with
-  // the 128-byte swizzle (the layout the TMA boxes produce)
-  const int chunk = col_elem >> 6, piece = (col_elem & 63) >> 3;
+// 16-bit element (row, col) -> byte offset in a [D/64][16 rows][128 B] tile
+// with the 128-byte swizzle (the layout the TMA boxes produce).
+__device__ __forceinline__ uint32_t swz16(int row, int col) {
+  const int chunk = col >> 6, piece = (col & 63) >> 3;
   return (uint32_t)(chunk * 2048 + row * 128 + ((piece ^ (row & 7)) << 4));
+}
+// fp8 byte (row, col) -> byte offset in a [D/128][16 rows][128 B] tile, same swizzle.
+__device__ __forceinline__ uint32_t swz8(int row, int col) {
+  const int chunk = col >> 7, piece = (col & 127) >> 4;
+  return (uint32_t)(chunk * 2048 + row * 128 + ((piece ^ (row & 7)) << 4) + (col & 15));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 
 struct Item {
@@ -96,12 +138,12 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
   return true;
 }
 
-template <typename T, int D>
+template <typename T, bool KV8, int D>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     decode_tma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, int total_items, int n_mblk,
                       uint32_t* counters) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, KV8>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -111,11 +153,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  const uint32_t wbase = base + warp * C::WARP_BYTES;   // this warp's slots, then its Q
-  const uint32_t sQ = wbase + NS * C::SLOT;
+  const uint32_t wring = base + warp * NS * C::SLOT;       // this warp's slots
+  const uint32_t sStg = base + C::OFF_AUX + warp * C::AUX; // fp8: widened V
+  const uint32_t sQ = sStg + C::STG;                       // the item's 16 query rows
   const uint32_t bar0 = base + C::OFF_BAR + warp * NS * 8;
   int2* meta = reinterpret_cast<int2*>(smem + C::OFF_META) + warp * NS;
-  volatile int abort_local = 0;  // per-warp: a timed-out wait ends this warp's work
+  volatile int abort_local = 0;  // a timed-out wait ends this warp's work
 
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -129,7 +172,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   int cur_id = -1, cur_chunk = 0;
   Item cur{};
   auto fetch = [&]() {
-    // lane 0: next non-empty item, or -1
+    // next non-empty item, or -1
     for (;;) {
       const int id = (int)atomicAdd(counters, 1u);
       if (id >= total_items) return -1;
@@ -137,7 +180,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     }
   };
   auto issue = [&](int s) {
-    // lane 0: put the cursor's next 16-key slot into ring slot s (or mark end)
+    // the cursor's next 16-key slot into ring slot s (or mark the end)
     if (cur_id < 0) {
       meta[s] = make_int2(-1, 0);
       return;
@@ -148,17 +191,17 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     const uint32_t bar = bar0 + 8 * s;
     if (page < 0 || page >= p.num_pages) {
       atomicOr(p.err, PA_DEVERR_BAD_PAGE);
-      meta[s] = make_int2(cur_id, cur_chunk | (1 << 30));  // consumer zero-fills
+      meta[s] = make_int2(cur_id, cur_chunk | (1 << 30));  // the consumer zero-fills
       mbar_arrive(bar);
     } else {
       const int tok0 = page * p.page_size + (s0 % p.page_size);
       meta[s] = make_int2(cur_id, cur_chunk);
       mbar_arrive_expect_tx(bar, C::SLOT);
-      const uint32_t dK = wbase + s * C::SLOT, dV = dK + C::HALF;
+      const uint32_t dK = wring + s * C::SLOT, dV = dK + C::HALF;
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(dK + c * 2048, &tmK, c * 64, cur.kh, tok0, bar);
-        tma_load_3d(dV + c * 2048, &tmV, c * 64, cur.kh, tok0, bar);
+        tma_load_3d(dK + c * 2048, &tmK, c * (128 / C::ELT), cur.kh, tok0, bar);
+        tma_load_3d(dV + c * 2048, &tmV, c * (128 / C::ELT), cur.kh, tok0, bar);
       }
     }
     if (++cur_chunk >= cur.nchunks) {
@@ -172,13 +215,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   }
   __syncwarp();
 
-  // ---- consumer ---------------------------------------------------------------
+  // ---- consumer -------------------------------------------------------------
   uint32_t phase = 0;  // bit s: parity of ring slot s
   int it_id = -1;
   Item f{};
   int last[2] = {-1, -1};
   float o[D / 8][4];
-  float m_run[2], l_run[2];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   const float sl2 = p.sl2;
   for (int s = 0;; s = (s + 1 == NS ? 0 : s + 1)) {
     // refill the slot consumed by the previous iteration (at the start: the
@@ -192,7 +235,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     const int chunk = mt.y & 0xFFFF;
     const bool bad = (mt.y >> 30) & 1;
     if (mt.x != it_id) {
-      // a new item: its rows' queries into the swizzled Q tile, fresh state
+      // a new item: its rows' queries into the Q tile, fresh state
       it_id = mt.x;
       item_info(a, it_id, n_mblk, f);
       for (int e = lane; e < 16 * (D / 8); e += 32) {
@@ -204,7 +247,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
                          ((int64_t)(f.qs + R / p.g) * p.hq + f.kh * p.g + R % p.g) * D + c8 * 8;
           v = __ldg(reinterpret_cast<const uint4*>(src));
         }
-        *reinterpret_cast<uint4*>(smem + (sQ - base) + swz_chunked(r, c8 * 8)) = v;
+        st_shared_v4(sQ + (KV8 ? (uint32_t)(r * C::QROW + c8 * 16) : swz16(r, c8 * 8)), v);
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -216,30 +259,60 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
     }
-    const uint32_t sK = wbase + s * C::SLOT, sV = sK + C::HALF;
+    const uint32_t sK = wring + s * C::SLOT, sV = sK + C::HALF;
     const int kb = f.k0 + 16 * chunk;
     const int nvalid = bad ? 0 : min(16, f.L - kb);
     if (nvalid < 16) {
       // keys past the row's end (or behind a bad table entry): zero their
       // K and V rows so stale or poisoned bytes never reach the products
-      for (int e = lane; e < (16 - nvalid) * 2 * (D / 8); e += 32) {
+      constexpr int PIECES = D * C::ELT / 16;  // 16-byte pieces per key row
+      for (int e = lane; e < (16 - nvalid) * 2 * PIECES; e += 32) {
         const int kv = e & 1, rest = e >> 1;
-        const int r = nvalid + rest / (D / 8), c8 = rest % (D / 8);
-        *reinterpret_cast<uint4*>(smem + ((kv ? sV : sK) - base) + swz_chunked(r, c8 * 8)) =
-            make_uint4(0u, 0u, 0u, 0u);
+        const int r = nvalid + rest / PIECES, pc = rest % PIECES;
+        const uint32_t off = KV8 ? swz8(r, pc * 16) : swz16(r, pc * 8);
+        st_shared_v4((kv ? sV : sK) + off, make_uint4(0u, 0u, 0u, 0u));
       }
     }
     __syncwarp();
+    uint32_t sVf = sV;  // 16-bit V tile the PV fragments come from
+    if (KV8) {
+      // widen this slot's V codes into the 16-bit staging tile
+      for (int e = lane; e < 16 * (D / 16); e += 32) {
+        const int r = e / (D / 16), pc = e % (D / 16);
+        const uint4 w = ld_shared_v4(sV + swz8(r, pc * 16));
+        uint4 lo, hi;
+        e5m2x4_to<T>(w.x, lo.x, lo.y);
+        e5m2x4_to<T>(w.y, lo.z, lo.w);
+        e5m2x4_to<T>(w.z, hi.x, hi.y);
+        e5m2x4_to<T>(w.w, hi.z, hi.w);
+        st_shared_v4(sStg + swz16(r, pc * 16), lo);
+        st_shared_v4(sStg + swz16(r, pc * 16 + 8), hi);
+      }
+      __syncwarp();
+      sVf = sStg;
+    }
 
     // S = Q K^T: 16 rows x 16 keys
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int kd = 0; kd < D / 16; ++kd) {
       uint32_t af[4], b0, b1, b2, b3;
-      ldsm_x4(sQ + swz_chunked(lane & 15, kd * 16 + (lane >> 4) * 8), af[0], af[1], af[2],
-              af[3]);
-      ldsm_x4(sK + swz_chunked((lane & 7) + ((lane >> 4) << 3), kd * 16 + ((lane >> 3) & 1) * 8),
-              b0, b1, b2, b3);
+      if (KV8) {
+        // reduction index permuted within each 16-wide step: operand slots
+        // (2t, 2t+1 | 2t+8, 2t+9) hold head-dim columns 4t .. 4t+3
+        const uint2 q0 = ld_shared_v2(sQ + gid * C::QROW + (kd * 16 + 4 * tig) * 2);
+        const uint2 q1 = ld_shared_v2(sQ + (gid + 8) * C::QROW + (kd * 16 + 4 * tig) * 2);
+        af[0] = q0.x;
+        af[1] = q1.x;
+        af[2] = q0.y;
+        af[3] = q1.y;
+        e5m2x4_to<T>(ld_shared_u32(sK + swz8(gid, kd * 16 + 4 * tig)), b0, b1);
+        e5m2x4_to<T>(ld_shared_u32(sK + swz8(gid + 8, kd * 16 + 4 * tig)), b2, b3);
+      } else {
+        ldsm_x4(sQ + swz16(lane & 15, kd * 16 + (lane >> 4) * 8), af[0], af[1], af[2], af[3]);
+        ldsm_x4(sK + swz16((lane & 7) + ((lane >> 4) << 3), kd * 16 + ((lane >> 3) & 1) * 8), b0,
+                b1, b2, b3);
+      }
       mma16816<T>(sc[0], af, b0, b1);
       mma16816<T>(sc[1], af, b2, b3);
     }
@@ -294,8 +367,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
 #pragma unroll
     for (int nd = 0; nd < D / 16; ++nd) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sV + swz_chunked((lane & 7) + (((lane >> 3) & 1) << 3), nd * 16 + (lane >> 4) * 8),
-                b0, b1, b2, b3);
+      ldsm_x4_t(sVf + swz16((lane & 7) + (((lane >> 3) & 1) << 3), nd * 16 + (lane >> 4) * 8), b0,
+                b1, b2, b3);
       mma16816<T>(o[2 * nd], pf, b0, b1);
       mma16816<T>(o[2 * nd + 1], pf, b2, b3);
     }
@@ -327,7 +400,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     __syncwarp();
   }
 
-  // a timed-out warp still has copies landing: let them finish before exit
+  // a timed-out warp may still have copies landing: let them finish
   if (abort_local) {
     for (int s = 0; s < NS; ++s)
       if (meta[s].x >= 0) mbar_drain(bar0 + 8 * s, (phase >> s) & 1u, p.err);
@@ -345,18 +418,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   }
 }
 
-}  // namespace
-
-bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
-  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype &&
-         (d == 64 || d == 128 || d == 256) && cache_tokens < (int64_t(1) << 31);
-}
-
-template <typename T, int D>
-static cudaError_t launch_dec(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                              int total_items, int n_mblk, uint32_t* counters, cudaStream_t st) {
-  using C = DecCfg<D>;
-  auto k = decode_tma_kernel<T, D>;
+template <typename T, bool KV8, int D>
+cudaError_t launch_dec(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                       int total_items, int n_mblk, uint32_t* counters, cudaStream_t st) {
+  using C = DecCfg<D, KV8>;
+  auto k = decode_tma_kernel<T, KV8, D>;
   static DeviceFlags attr;
   cudaError_t e = attr.once([&] {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -372,26 +438,44 @@ static cudaError_t launch_dec(const AttnArgs& a, const CUtensorMap& tk, const CU
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int n_mblk, cudaStream_t st) {
+template <typename T, bool KV8>
+cudaError_t launch_dec_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                         int items, int n_mblk, uint32_t* cnt, cudaStream_t st) {
+  switch (a.p.d) {
+    case 64:
+      if constexpr (!KV8) return launch_dec<T, KV8, 64>(a, tk, tv, items, n_mblk, cnt, st);
+      break;
+    case 128: return launch_dec<T, KV8, 128>(a, tk, tv, items, n_mblk, cnt, st);
+    case 256: return launch_dec<T, KV8, 256>(a, tk, tv, items, n_mblk, cnt, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
+  if (!(q_dtype == PA_BF16 || q_dtype == PA_F16) || cache_tokens >= (int64_t(1) << 31)) return false;
+  if (kv_dtype == q_dtype) return d == 64 || d == 128 || d == 256;
+  return kv_dtype == PA_E5M2 && (d == 128 || d == 256);
+}
+
+cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
+                              cudaStream_t st) {
   if (a.p.num_rows == 0 || n_mblk == 0) return cudaSuccess;
   const int64_t items = (int64_t)a.p.num_rows * a.p.hkv * NSPLIT * n_mblk;
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;
-  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+  if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
   uint32_t* counters = reinterpret_cast<WsHeader*>(a.p.err)->pad;
-  const bool bf = q_dtype == PA_BF16;
-  switch (a.p.d) {
-    case 64: return bf ? launch_dec<__nv_bfloat16, 64>(a, tk, tv, (int)items, n_mblk, counters, st)
-                       : launch_dec<__half, 64>(a, tk, tv, (int)items, n_mblk, counters, st);
-    case 128: return bf ? launch_dec<__nv_bfloat16, 128>(a, tk, tv, (int)items, n_mblk, counters, st)
-                        : launch_dec<__half, 128>(a, tk, tv, (int)items, n_mblk, counters, st);
-    case 256: return bf ? launch_dec<__nv_bfloat16, 256>(a, tk, tv, (int)items, n_mblk, counters, st)
-                        : launch_dec<__half, 256>(a, tk, tv, (int)items, n_mblk, counters, st);
-  }
-  return cudaErrorInvalidValue;
+  const bool kv8 = kv_dtype == PA_E5M2;
+  if (q_dtype == PA_BF16)
+    return kv8 ? launch_dec_d<__nv_bfloat16, true>(a, tk, tv, (int)items, n_mblk, counters, st)
+               : launch_dec_d<__nv_bfloat16, false>(a, tk, tv, (int)items, n_mblk, counters, st);
+  return kv8 ? launch_dec_d<__half, true>(a, tk, tv, (int)items, n_mblk, counters, st)
+             : launch_dec_d<__half, false>(a, tk, tv, (int)items, n_mblk, counters, st);
 }
 
 }  // namespace pa

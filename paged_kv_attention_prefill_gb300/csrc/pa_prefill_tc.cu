@@ -453,17 +453,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 64 elements.
-bool encode_kv_map(CUtensorMap* tm, const void* cache, int q_dtype, int d, int hkv,
+// [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 128 bytes
+// (64 16-bit elements or 128 fp8 codes), 128-byte swizzle.
+bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
                    int64_t tokens) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const int elt = kv_dtype == PA_E5M2 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)tokens};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hkv * d * 2};
-  cuuint32_t box[3] = {64, 1, 16};
+  cuuint64_t strides[2] = {(cuuint64_t)d * elt, (cuuint64_t)hkv * d * elt};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), 1, 16};
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      q_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt = kv_dtype == PA_E5M2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return fn(tm, dt, 3, const_cast<void*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
