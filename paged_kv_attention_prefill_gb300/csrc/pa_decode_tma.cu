@@ -52,8 +52,7 @@ struct DecCfg {
   static constexpr uint32_t SLOT = 2 * HALF;
   static constexpr int NS = KV8 ? (D == 256 ? 5 : 8) : (D == 256 ? 3 : (D == 128 ? 6 : 8));
   static constexpr uint32_t STG = KV8 ? 16 * D * 2 : 0;    // widened V of one slot
-  static constexpr uint32_t QROW = KV8 ? D * 2 + 16 : D * 2;  // fp8: padded, unswizzled rows
-  static constexpr uint32_t QB = 16 * QROW;
+  static constexpr uint32_t QB = 16 * D * 2;
   static constexpr uint32_t AUX = STG + QB;
   static constexpr uint32_t OFF_AUX = DEC_WARPS * NS * SLOT;  // all rings first (1 KB aligned)
   static constexpr uint32_t OFF_BAR = OFF_AUX + DEC_WARPS * AUX;
@@ -69,6 +68,13 @@ struct DecCfg {
 __device__ __forceinline__ uint32_t swz16(int row, int col) {
   const int chunk = col >> 6, piece = (col & 63) >> 3;
   return (uint32_t)(chunk * 2048 + row * 128 + ((piece ^ (row & 7)) << 4));
+}
+// Q tile of the fp8 path: rows of D 16-bit values, 8-byte units XOR-swizzled
+// by row so the permuted 64-bit operand loads of 16 lanes hit 32 banks.
+template <int D>
+__device__ __forceinline__ uint32_t qswz8(int row, int col) {
+  const int unit = (col >> 2) ^ ((row & 7) << 2);
+  return (uint32_t)(row * D * 2 + unit * 8 + (col & 3) * 2);
 }
 // fp8 byte (row, col) -> byte offset in a [D/128][16 rows][128 B] tile, same swizzle.
 __device__ __forceinline__ uint32_t swz8(int row, int col) {
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
                          ((int64_t)(f.qs + R / p.g) * p.hq + f.kh * p.g + R % p.g) * D + c8 * 8;
           v = __ldg(reinterpret_cast<const uint4*>(src));
         }
-        st_shared_v4(sQ + (KV8 ? (uint32_t)(r * C::QROW + c8 * 16) : swz16(r, c8 * 8)), v);
+        st_shared_v4(sQ + (KV8 ? qswz8<D>(r, c8 * 8) : swz16(r, c8 * 8)), v);
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -278,7 +284,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     if (KV8) {
       // widen this slot's V codes into the 16-bit staging tile
       for (int e = lane; e < 16 * (D / 16); e += 32) {
-        const int r = e / (D / 16), pc = e % (D / 16);
+        const int r = e & 15, pc = e >> 4;  // 8 lanes of a quarter-warp: 8 rows, one piece
         const uint4 w = ld_shared_v4(sV + swz8(r, pc * 16));
         uint4 lo, hi;
         e5m2x4_to<T>(w.x, lo.x, lo.y);
@@ -300,8 +306,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
       if (KV8) {
         // reduction index permuted within each 16-wide step: operand slots
         // (2t, 2t+1 | 2t+8, 2t+9) hold head-dim columns 4t .. 4t+3
-        const uint2 q0 = ld_shared_v2(sQ + gid * C::QROW + (kd * 16 + 4 * tig) * 2);
-        const uint2 q1 = ld_shared_v2(sQ + (gid + 8) * C::QROW + (kd * 16 + 4 * tig) * 2);
+        const uint2 q0 = ld_shared_v2(sQ + qswz8<D>(gid, kd * 16 + 4 * tig));
+        const uint2 q1 = ld_shared_v2(sQ + qswz8<D>(gid + 8, kd * 16 + 4 * tig));
         af[0] = q0.x;
         af[1] = q1.x;
         af[2] = q0.y;
