@@ -181,6 +181,36 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
                            const void* k_cache, const void* v_cache, void* out,
                            void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
+/*
+ * Split-KV decode that allocates nothing and takes no workspace.
+ *
+ * No counterpart on the pages: this is an addition for callers that cannot
+ * allocate device memory -- for example a plugin loaded into a program that
+ * has already reserved all device memory for its own pool, or a plain C host
+ * that must keep its device memory use fixed after start-up and has no
+ * allocator to own a workspace's lifetime.
+ *
+ * Same arguments, layouts and results as paged_attn_decode minus the
+ * workspace.  The scratch it needs (the fp32 partial states and a small
+ * header) is one array of PA_STATIC_SCRATCH_BYTES that the library keeps in
+ * device memory: every GPU that loads the library holds it until the process
+ * exits.  A batch whose paged_attn_workspace_size() exceeds that size is
+ * rejected with PA_ERR_WORKSPACE_TOO_SMALL before anything is launched (use
+ * paged_attn_decode with a workspace of your own for larger batches).  The
+ * call never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * The first call on a device does a one-time set-up (it looks up the array's
+ * device address with that device current); make that first call before any
+ * stream capture.  Every call shares the one array: calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race and may
+ * corrupt each other's results -- serialize them.  Each call clears the
+ * array's header; device-side error flags are not reported by this call.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+pa_status paged_attn_decode_static(const pa_params* params, const pa_batch* batch, const void* q,
+                                   const void* k_cache, const void* v_cache, void* out,
+                                   pa_stream_t stream);
+
 /* Error flags the kernels may set in the workspace header (sticky). */
 #define PA_DEVERR_BAD_PAGE   0x1u  /* a needed block-table entry outside [0, num_pages),
                                       or a key past the row's block-table columns */

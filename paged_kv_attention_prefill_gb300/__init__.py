@@ -23,11 +23,13 @@ from typing import Optional
 
 import torch
 
-__all__ = ["paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed", "workspace_size",
+__all__ = ["paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed",
+           "paged_attn_decode_static", "STATIC_SCRATCH_BYTES", "workspace_size",
            "make_workspace", "read_errors", "load", "PagedAttnError", "library_path",
            "PA_F32", "PA_F16", "PA_BF16", "PA_E5M2"]
 
 PA_F32, PA_F16, PA_BF16, PA_E5M2 = 0, 1, 2, 3
+STATIC_SCRATCH_BYTES = 16 << 20  # PA_STATIC_SCRATCH_BYTES of include/paged_attn.h
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small",
            4: "CUDA error", 5: "no sm_103 device"}
 DEVERR = {1: "bad block-table entry", 4: "decode row q_len > max_decode_q"}
@@ -79,6 +81,10 @@ def load():
                 f.restype = ctypes.c_int
                 f.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            lib.paged_attn_decode_static.restype = ctypes.c_int
+            lib.paged_attn_decode_static.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p]
             lib.paged_attn_workspace_size.restype = ctypes.c_size_t
             lib.paged_attn_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.c_int32]
             lib.paged_attn_read_errors.restype = ctypes.c_int
@@ -186,6 +192,38 @@ def paged_attn_mixed(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *
     """Mixed batch: short rows to split-KV decode, the rest to prefill."""
     return _call("paged_attn_mixed", q, k_cache, v_cache, block_table, cu_seqlens_q,
                  seq_lens, **kw)
+
+
+def paged_attn_decode_static(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *,
+                             out=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0,
+                             max_decode_q=0, cu_seqlens_q_host=None, seq_lens_host=None,
+                             stream=None):
+    """Split-KV decode without a workspace: for callers that cannot allocate
+    device memory.  The library's fixed device array (STATIC_SCRATCH_BYTES,
+    shared by every call) holds the scratch; larger batches are refused.
+    Calls that overlap on the GPU race -- serialize them."""
+    for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise PagedAttnError("all tensors must be contiguous CUDA tensors")
+    prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
+                      v_scale=v_scale, max_decode_q=max_decode_q)
+    B = int(seq_lens.shape[0])
+    if out is None:
+        out = torch.empty_like(q)
+    hcu = hl = None
+    if cu_seqlens_q_host is not None and seq_lens_host is not None:
+        hcu = torch.as_tensor(cu_seqlens_q_host, dtype=torch.int32).contiguous()
+        hl = torch.as_tensor(seq_lens_host, dtype=torch.int32).contiguous()
+    bat = Batch(B, int(q.shape[0]), int(k_cache.shape[0]), int(block_table.shape[1]) if B else 0,
+                _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(block_table), _ptr(hcu), _ptr(hl))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        rc = load().paged_attn_decode_static(ctypes.byref(prm), ctypes.byref(bat), _ptr(q),
+                                             _ptr(k_cache), _ptr(v_cache), _ptr(out), sp)
+    _check_status(rc, "paged_attn_decode_static")
+    return out
 
 
 def read_errors(workspace: torch.Tensor, stream=None) -> int:

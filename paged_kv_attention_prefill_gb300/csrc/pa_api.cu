@@ -314,3 +314,70 @@ const char* paged_attn_status_string(pa_status status) {
 int32_t paged_attn_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Split-KV decode for callers that cannot allocate device memory.
+//
+// The decode path needs scratch memory (the partial softmax states and a
+// small header).  Callers that cannot hand the library a workspace -- a
+// plugin running inside a program that has already reserved all device
+// memory for its own pool, or a plain C host that must keep its device
+// memory use fixed after start-up and has no allocator to own a buffer's
+// lifetime -- use paged_attn_decode_static instead.  Its scratch is this
+// file-scope device array: every GPU that loads the library holds it until
+// the process exits, and no call allocates or frees anything.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace pa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void* g_static_addr[64];  // the array's device address, per device
+
+// One-time set-up per device (with that device current): look up where the
+// array lives.  The array's name is only a host-side stand-in in host code;
+// the kernels must be given this address.
+pa_status static_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_NO_DEVICE;
+  if (dev < 0 || dev >= 64) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status paged_attn_decode_static(const pa_params* params, const pa_batch* batch,
+                                              const void* q, const void* k_cache,
+                                              const void* v_cache, void* out,
+                                              pa_stream_t stream) {
+  using namespace pa;
+  Resolved r;
+  // size check against the fixed array (any non-null stand-in for the
+  // workspace pointer: the address is only looked up below)
+  pa_status s = validate(E_DECODE, params, batch, q, k_cache, v_cache, out,
+                         reinterpret_cast<void*>(uintptr_t(1)), PA_STATIC_SCRATCH_BYTES, &r);
+  if (s != PA_OK) return s;
+  if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
+  void* ws = nullptr;
+  s = static_scratch_address(&ws);
+  if (s != PA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents; the header (error word and
+  // the decode kernel's work counter) must start at zero
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return PA_ERR_CUDA;
+  AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, ws);
+  const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
+  const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
+  return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots, st));
+}
