@@ -19,12 +19,14 @@
 //    poisoned cache bytes ever reach the value product.
 //  * Warp 1, one elected thread, issues tcgen05.mma: S = Q K^T (M=128,
 //    N = key tile, K = d) into one of two TMEM buffers, and O += P V
-//    (N = d) into a TMEM accumulator.  Commits signal the other warps.
-//  * Warps 4-7 (one query row per TMEM lane) read S from TMEM, apply the
-//    causal mask, run the online softmax, write P (16-bit) into shared
-//    memory for the second MMA, rescale O in TMEM when the running maximum
-//    grows by more than 2^8 (otherwise the stale maximum is kept: the final
-//    O / l is unchanged), and finally normalise O and store the rows.
+//    (N = d, P read from TMEM) into a TMEM accumulator.  Commits signal the
+//    other warps.
+//  * Warps 4-11, two warpgroups sharing each query row (TMEM lane) by
+//    columns, read S from TMEM, apply the causal mask, run the online
+//    softmax, write P (16-bit) back into TMEM as the A operand of the second
+//    MMA (no shared-memory round trip), rescale O in TMEM when the running
+//    maximum grows by more than 2^8 (otherwise the stale maximum is kept: the
+//    final O / l is unchanged), and finally normalise O and store the rows.
 //
 // Every wait is bounded (about two seconds); a CTA that runs out sets a
 // workspace flag, drains its own copies and MMAs, frees TMEM and exits.
@@ -47,25 +49,25 @@ struct TcCfg {
   // K is released as soon as S = Q K^T is done, V only after O += P V, so
   // the K ring runs further ahead than the V ring.
   static constexpr int KS = D == 64 ? 4 : (D == 128 ? 3 : 2);
-  static constexpr int VS = D == 64 ? 3 : 2;
+  static constexpr int VS = D == 64 ? 4 : 3;
   static constexpr int NCH = D / 64;                // 128-byte column chunks of d
   static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
   static constexpr uint32_t Q_BYTES = BM * D * 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one tile
-  static constexpr uint32_t P_BYTES = BM * BN * 2;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + VS * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
   static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t O_COL = 2 * BN;         // S double buffer in [0, 2 BN)
+  static constexpr uint32_t P_COL = O_COL + D;      // P (16-bit pairs): BN / 2 columns
+  static constexpr uint32_t XCH_COL = 448;          // 6 spare columns: softmax warpgroups' swaps
   // barrier indices
   static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
                        B_SF = 2 * KS + 2 * VS, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PV = B_PF + 1,
                        B_Q = B_PV + 1, B_DRAIN = B_Q + 1, NBAR = B_DRAIN + 1;
-  static_assert(O_COL + D <= TMEM_COLS, "TMEM budget");
+  static_assert(P_COL + BN / 2 <= XCH_COL && XCH_COL + 6 <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NBAR * 8 <= 192, "barrier area");
 };
@@ -84,7 +86,29 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
 }
 
 template <int N>
+__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&v)[N]);
+template <>
+__device__ __forceinline__ void tmem_st_row<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+  tmem_st_x32(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_st_row<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+  tmem_st_x16(taddr, v);
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <int N>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&x)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_row<32>(uint32_t taddr, float (&x)[32]) {
+  uint32_t r[32];
+  tmem_ld_x32(taddr, r);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r[k]);
+}
 template <>
 __device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, float (&x)[128]) {
   uint32_t r[128];
@@ -101,7 +125,7 @@ __device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, float (&x)[64]) 
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using C = TcCfg<D>;
@@ -109,8 +133,7 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V,
-                 sP = base + C::OFF_P;
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
   const uint32_t bar0 = base + C::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 196);
@@ -120,8 +143,10 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item (uniform over the CTA) -----------------------------------
-  // 1-D grid, KV head fastest: the (longest-first) work list is dispatched in order
-  const int item = blockIdx.x / p.hkv, kh = blockIdx.x % p.hkv;
+  // 1-D grid, KV head slowest: CTAs that run together read the same heads'
+  // K/V (L2 reuse); within a head the work list is longest-first
+  const int n_items = (int)(gridDim.x / p.hkv);
+  const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
   if (item >= (int)*a.n_tiles) return;
   const int2 wi = a.tiles[item];
   const int b = wi.x, mb = wi.y;
@@ -151,9 +176,9 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_SF + s), 1);
-      mbar_init(bar(C::B_SE + s), 128);
+      mbar_init(bar(C::B_SE + s), 256);
     }
-    mbar_init(bar(C::B_PF), 128);
+    mbar_init(bar(C::B_PF), 256);
     mbar_init(bar(C::B_PV), 1);
     mbar_init(bar(C::B_Q), 128);
     mbar_init(bar(C::B_DRAIN), 1);
@@ -280,10 +305,11 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < C::BN / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sP + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            // A = P straight from TMEM: 16 keys = 8 columns of 16-bit pairs
             const uint64_t bd =
                 sdesc_sw128(sV + stp * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-            tc_mma_f16(tmem + C::O_COL, ad, bd, idO, (jj > 0 || k > 0) ? 1u : 0u);
+            tc_mma_f16_ts(tmem + C::O_COL, tmem + C::P_COL + 8 * k, bd, idO,
+                          (jj > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(bar(C::B_PV));
           tc_commit(bar(C::B_VE + stp));
@@ -295,7 +321,17 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ============ softmax / correction / epilogue: one row per thread =======
+    // ============ softmax / correction / epilogue ==============================
+    // Two warpgroups share every tile row (TMEM lane): warpgroup hf (warps
+    // 4-7: hf = 0, warps 8-11: hf = 1) owns columns [hf BN/2, (hf+1) BN/2) of
+    // S and P and head-dim columns [hf d/2, (hf+1) d/2) of O.  Each tile they
+    // swap their partial row maxima through spare TMEM columns and a named
+    // barrier (so both take identical rescale decisions); each keeps its own
+    // partial row sum, added in a fixed order at the end.  This loop never
+    // leaves early: after a timed-out wait it runs on (flag raised, waits
+    // return at once) so both warpgroups always meet the same barriers.
+    constexpr int HN = C::BN / 2, HD = D / 2;
+    const int hf = warp >= 8 ? 1 : 0;
     const int q4 = warp & 3;          // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;     // tile row == TMEM lane
     const int R = R0 + r;
@@ -303,7 +339,7 @@ __global__ void __launch_bounds__(256, 1)
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
     const int last = valid ? L - qb + i : -1;  // last visible key of this row
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
-    {
+    if (hf == 0) {
       const T* qrow = static_cast<const T*>(a.q) + qoff;
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) {
@@ -320,29 +356,40 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     const float sl2 = p.sl2;
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int buf = j & 1;
-      ok = mbar_wait(bar(C::B_SF + buf), (j >> 1) & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
+      mbar_wait(bar(C::B_SF + buf), (j >> 1) & 1, abort_flag, p.err);
       tc_fence_after();
-      float x[C::BN];
-      tmem_ld_row<C::BN>(trow + buf * C::BN, x);
+      float x[HN];
+      tmem_ld_row<HN>(trow + buf * C::BN + hf * HN, x);
       tc_fence_before();
       mbar_arrive(bar(C::B_SE + buf));
 
-      const int kb = j * C::BN;
-      float mt = -INFINITY;  // max raw logit of the tile (masked keys -> -inf)
-      if (kb + C::BN - 1 > last) {
+      const int kb = j * C::BN + hf * HN;
+      if (kb + HN - 1 > last) {
 #pragma unroll
-        for (int k = 0; k < C::BN; ++k)
+        for (int k = 0; k < HN; ++k)
           if (kb + k > last) x[k] = -INFINITY;
       }
+      float mt = -INFINITY;  // max raw logit of this half tile (masked keys -> -inf)
+      {
+        float pm[8];
 #pragma unroll
-      for (int k = 0; k < C::BN; ++k) mt = fmaxf(mt, x[k]);
+        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+#pragma unroll
+        for (int k = 8; k < HN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mt = fmaxf(mt, pm[u]);
+      }
+      {  // swap partial maxima with the other warpgroup
+        uint32_t v[1] = {__float_as_uint(mt)};
+        tmem_st_x1(trow + C::XCH_COL + 2 * buf + hf, v);
+        tc_fence_before();
+        named_bar_sync(1, 256);
+        tc_fence_after();
+        tmem_ld_x1(trow + C::XCH_COL + 2 * buf + (hf ^ 1), v);
+        mt = fmaxf(mt, __uint_as_float(v[0]));
+      }
       const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
       float factor = 1.f;
       bool need = false;
@@ -354,74 +401,78 @@ __global__ void __launch_bounds__(256, 1)
         m_used = m_new;
       }
       const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-      float rs = 0.f;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
 #pragma unroll
-      for (int k = 0; k < C::BN; ++k) {
+      for (int k = 0; k < HN; ++k) {
         x[k] = ex2(fmaf(x[k], sl2, nmu));
-        rs += x[k];
+        ps[k & 7] += x[k];
       }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       // the previous tile's P V must be done: O is stable and P's buffer free
       if (j >= 1) {
-        ok = mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+        mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
-          tmem_ld_x32(trow + C::O_COL + c * 32, o);
+          tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
-          tmem_st_x32(trow + C::O_COL + c * 32, o);
+          tmem_st_x32(trow + C::O_COL + hf * HD + c * 32, o);
         }
       }
       l = l * factor + rs;
+      {
+        // P (16-bit pairs) into TMEM: this warpgroup's HN keys = HN / 2 columns
+        uint32_t pk[HN / 2];
 #pragma unroll
-      for (int pc = 0; pc < C::BN / 8; ++pc) {
-        uint4 v;
-        v.x = pack2<T>(x[8 * pc + 0], x[8 * pc + 1]);
-        v.y = pack2<T>(x[8 * pc + 2], x[8 * pc + 3]);
-        v.z = pack2<T>(x[8 * pc + 4], x[8 * pc + 5]);
-        v.w = pack2<T>(x[8 * pc + 6], x[8 * pc + 7]);
-        const int c = pc >> 3, piece = pc & 7;
-        st_shared_v4(sP + c * (C::BM * 128) + r * 128 + ((piece ^ (r & 7)) << 4), v);
+        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
+        tmem_st_row<HN / 2>(trow + C::P_COL + hf * (HN / 2), pk);
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::B_PF));
     }
-    // ---- epilogue: out = O / l * v_scale ----
-    T* orow = static_cast<T*>(a.out) + qoff;
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        const float inv = l > 0.f ? p.v_scale / l : 0.f;
+    // ---- epilogue: out = O / (l_0 + l_1) * v_scale ----
+    if (n_tiles > 0) {
+      mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
+      tc_fence_after();
+    }
+    float lt;
+    {
+      uint32_t v[1] = {__float_as_uint(l)};
+      tmem_st_x1(trow + C::XCH_COL + 4 + hf, v);
+      tc_fence_before();
+      named_bar_sync(1, 256);
+      tc_fence_after();
+      tmem_ld_x1(trow + C::XCH_COL + 4 + (hf ^ 1), v);
+      const float lo = __uint_as_float(v[0]);
+      lt = hf == 0 ? l + lo : lo + l;  // the same sum in both warpgroups
+    }
+    T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
+    if (n_tiles > 0) {
+      const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld_x32(trow + C::O_COL + c * 32, o);
-          if (valid) {
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
+        if (valid) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 v;
-              v.x = pack2<T>(__uint_as_float(o[8 * w + 0]) * inv, __uint_as_float(o[8 * w + 1]) * inv);
-              v.y = pack2<T>(__uint_as_float(o[8 * w + 2]) * inv, __uint_as_float(o[8 * w + 3]) * inv);
-              v.z = pack2<T>(__uint_as_float(o[8 * w + 4]) * inv, __uint_as_float(o[8 * w + 5]) * inv);
-              v.w = pack2<T>(__uint_as_float(o[8 * w + 6]) * inv, __uint_as_float(o[8 * w + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c * 32 + 8 * w) = v;
-            }
+          for (int w = 0; w < 4; ++w) {
+            uint4 v;
+            v.x = pack2<T>(__uint_as_float(o[8 * w + 0]) * inv, __uint_as_float(o[8 * w + 1]) * inv);
+            v.y = pack2<T>(__uint_as_float(o[8 * w + 2]) * inv, __uint_as_float(o[8 * w + 3]) * inv);
+            v.z = pack2<T>(__uint_as_float(o[8 * w + 4]) * inv, __uint_as_float(o[8 * w + 5]) * inv);
+            v.w = pack2<T>(__uint_as_float(o[8 * w + 6]) * inv, __uint_as_float(o[8 * w + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * w) = v;
           }
         }
       }
-    } else if (ok && valid) {
+    } else if (valid) {
       // no key visible to any row of the tile
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c)
+      for (int c = 0; c < HD / 8; ++c)
         *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
@@ -484,7 +535,7 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMa
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), 256, C::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, C::SMEM, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
