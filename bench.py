@@ -45,6 +45,30 @@ HEADLINE_WORKLOAD = 2
 L2_BYTES = 129 * 1024 * 1024
 
 
+# DRAM bytes (read + write) per launch of the prefill kernel on this workload,
+# from the ncu capture summarised in profiles/prefill_tc_workload2.md.  Reported
+# only while the kernel's sources are the ones that were profiled.
+PROFILED_PREFILL_TRAFFIC = {
+    "sources": {
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc.cu": "83ee3f6ef78ac3df5867f9cd9623edd8e6a87deeec98749a1e0460c8311f0fed",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "a0c3f742d599cb59e88fbba788f02b84fb6cdc49843e0cc8eda785ab5bf4decd",
+    },
+    "bytes_per_launch": 465146624,
+}
+
+
+def profiled_traffic():
+    import hashlib
+    for rel, digest in PROFILED_PREFILL_TRAFFIC["sources"].items():
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return PROFILED_PREFILL_TRAFFIC["bytes_per_launch"]
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -334,7 +358,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world} (rows independent)"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                          "peak": pk["bf16"], "unit": "TFLOP/s",
-                         "frac": round(achieved / pk["bf16"], 4), "traffic": None,
+                         "frac": round(achieved / pk["bf16"], 4), "traffic": profiled_traffic(),
                          "kernel": "prefill (whole call timed: routing kernel included)",
                          "peak_source": f"{pk['source']} bf16 burst"},
             "cpu_baseline": {"value": round(cpu_val, 6), "unit": "TFLOP/s", "cores": cores,
