@@ -12,19 +12,25 @@
 //    box per 128 bytes of a key row, for K and for V, straight from the
 //    block table into the warp's private ring of NS slots.  The warp keeps
 //    NS-1 slots in flight and prefetches across item boundaries, so HBM
-//    never waits for a warp to start its next item.
-//  * The math per slot is warp-level MMA (m16n8k16): S = Q K^T for the 16
-//    rows x 16 keys, the online softmax in registers, O += P V.  At the end
-//    of an item the warp writes (acc[d], m, l) of its rows for that split.
+//    never waits for a warp to start its next item.  Eight warps per CTA
+//    (four for 16 KB slots) give each SM sub-partition two independent
+//    chains of dependent work to interleave.
+//  * The math per slot is warp-level MMA (m16n8k16) on the transposed
+//    products, keys on the M side: S^T = K Q^T, then O^T += V^T P^T.  Q is
+//    the B operand of S^T and lives in registers for the whole item; K and
+//    V are read once each with ldmatrix (V transposed by ldmatrix itself);
+//    P^T is S^T's accumulator moved across lanes with movmatrix.  The
+//    online softmax reduces over the 8 lanes that share a query row, and a
+//    row's exponent reference moves only when its maximum passes it by more
+//    than a factor of 256, so O^T is rarely rescaled.  At the end of an item
+//    the warp writes (acc[d], m, l) of its rows for that split.
 //  * fp8 E5M2 caches (1Cat-vLLM PR #616, original description: an fp8_e5m2
 //    KV cache dequantized in the kernel): an E5M2 code in the high byte of a
-//    16-bit word is the same binary16 value, so K is widened straight from
-//    the raw slot into MMA operands -- four consecutive codes of one key
-//    become two fp16 pairs, and Q's reduction index is permuted the same way
-//    so the dot product is unchanged -- while V is widened once per slot
-//    into a 16-bit staging tile for the transposed fragment loads.  The
-//    per-tensor k_scale is folded into the logit scale, v_scale into the
-//    merge.
+//    16-bit word is the same binary16 value.  K words of four codes widen
+//    into two binary16 pairs (Q's reduction index is permuted to match);
+//    V is loaded by ldmatrix.trans as code pairs of two keys, and one byte
+//    permute per operand register places the codes.  The per-tensor k_scale
+//    is folded into the logit scale, v_scale into the merge.
 //  * No block-wide barrier anywhere: warps only wait on their own mbarriers.
 //    All waits are clock-bounded.
 //
@@ -42,44 +48,30 @@ namespace {
 
 using namespace sm100;
 
-constexpr int DEC_WARPS = 4;
-
 template <int D, bool KV8>
 struct DecCfg {
   static constexpr int ELT = KV8 ? 1 : 2;
   static constexpr int NCH = D * ELT / 128;                // 128-byte boxes per key row
+  static constexpr int SEGS = D * ELT / 16;                // 16-byte segments per key row
   static constexpr uint32_t HALF = 16 * D * ELT;           // K (or V) of one 16-key slot
   static constexpr uint32_t SLOT = 2 * HALF;
-  static constexpr int NS = KV8 ? (D == 256 ? 5 : 8) : (D == 256 ? 3 : (D == 128 ? 6 : 8));
-  static constexpr uint32_t STG = KV8 ? 16 * D * 2 : 0;    // widened V of one slot
-  static constexpr uint32_t QB = 16 * D * 2;
-  static constexpr uint32_t AUX = STG + QB;
-  static constexpr uint32_t OFF_AUX = DEC_WARPS * NS * SLOT;  // all rings first (1 KB aligned)
-  static constexpr uint32_t OFF_BAR = OFF_AUX + DEC_WARPS * AUX;
-  static constexpr uint32_t OFF_META = OFF_BAR + DEC_WARPS * NS * 8;
-  static constexpr uint32_t SMEM = OFF_META + DEC_WARPS * NS * 8 + 1024;
+  static constexpr int W = SLOT >= 16384 ? 4 : 8;          // warps per CTA, one ring each
+  static constexpr int NS_FIT = (224 * 1024) / (W * SLOT);
+  static constexpr int NS = NS_FIT < 16 ? NS_FIT : 16;     // ring slots per warp
+  static constexpr uint32_t OFF_BAR = W * NS * SLOT;       // all rings first (1 KB aligned)
+  static constexpr uint32_t OFF_META = OFF_BAR + W * NS * 8;
+  static constexpr uint32_t SMEM = OFF_META + W * NS * 8 + 1024;
   static_assert(SLOT % 1024 == 0, "slot alignment");
-  static_assert(AUX % 16 == 0, "aux alignment");
+  static_assert(NS >= 3, "ring depth");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// 16-bit element (row, col) -> byte offset in a [D/64][16 rows][128 B] tile
-// with the 128-byte swizzle (the layout the TMA boxes produce).
-__device__ __forceinline__ uint32_t swz16(int row, int col) {
-  const int chunk = col >> 6, piece = (col & 63) >> 3;
-  return (uint32_t)(chunk * 2048 + row * 128 + ((piece ^ (row & 7)) << 4));
-}
-// Q tile of the fp8 path: rows of D 16-bit values, 8-byte units XOR-swizzled
-// by row so the permuted 64-bit operand loads of 16 lanes hit 32 banks.
-template <int D>
-__device__ __forceinline__ uint32_t qswz8(int row, int col) {
-  const int unit = (col >> 2) ^ ((row & 7) << 2);
-  return (uint32_t)(row * D * 2 + unit * 8 + (col & 3) * 2);
-}
-// fp8 byte (row, col) -> byte offset in a [D/128][16 rows][128 B] tile, same swizzle.
-__device__ __forceinline__ uint32_t swz8(int row, int col) {
-  const int chunk = col >> 7, piece = (col & 127) >> 4;
-  return (uint32_t)(chunk * 2048 + row * 128 + ((piece ^ (row & 7)) << 4) + (col & 15));
+// Byte offset of 16-byte segment `seg` of key row `key` (0..15) in a slot
+// half: [segs / 8][16 rows][128 B] with the 128-byte swizzle the TMA boxes
+// produce (16-byte unit index XOR row % 8).  Eight consecutive rows at one
+// segment fall in eight different bank groups.
+__device__ __forceinline__ uint32_t seg_off(int key, int seg) {
+  return (uint32_t)((seg >> 3) * 2048 + key * 128 + (((seg & 7) ^ (key & 7)) << 4));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -87,23 +79,26 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+
+// 8x8 transpose of 16-bit elements across the warp: lane (g, t) gives
+// M[g][2t..2t+1] and receives M[2t][g], M[2t+1][g].
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
 }
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
-  return v;
+
+// A binary16 pair (as produced from E5M2 codes) in the compute type.
+template <typename T>
+__device__ __forceinline__ uint32_t h2_to(uint32_t h);
+template <>
+__device__ __forceinline__ uint32_t h2_to<__half>(uint32_t h) {
+  return h;
 }
-__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-  return v;
+template <>
+__device__ __forceinline__ uint32_t h2_to<__nv_bfloat16>(uint32_t h) {
+  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  return pack2<__nv_bfloat16>(f.x, f.y);
 }
 
 struct Item {
@@ -145,12 +140,14 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
 }
 
 template <typename T, bool KV8, int D>
-__global__ void __launch_bounds__(DEC_WARPS * 32, 1)
+__global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
     decode_tma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, int total_items, int n_mblk,
                       uint32_t* counters) {
   using C = DecCfg<D, KV8>;
   constexpr int NS = C::NS;
+  constexpr int KSTEPS = D / 16;  // 16-wide reduction steps of S over the head dim
+  constexpr int MT = D / 16;      // 16-row tiles of O^T over the head dim
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -159,9 +156,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  const uint32_t wring = base + warp * NS * C::SLOT;       // this warp's slots
-  const uint32_t sStg = base + C::OFF_AUX + warp * C::AUX; // fp8: widened V
-  const uint32_t sQ = sStg + C::STG;                       // the item's 16 query rows
+  const uint32_t wring = base + warp * NS * C::SLOT;  // this warp's slots
   const uint32_t bar0 = base + C::OFF_BAR + warp * NS * 8;
   int2* meta = reinterpret_cast<int2*>(smem + C::OFF_META) + warp * NS;
   volatile int abort_local = 0;  // a timed-out wait ends this warp's work
@@ -222,13 +217,34 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   __syncwarp();
 
   // ---- consumer -------------------------------------------------------------
+  // The warp computes the transposed products, keys on the MMA's M side:
+  //   S^T[16 keys x 16 rows]  = K[16 x d] . Q^T[d x 16]
+  //   O^T[d x 16 rows]       += V^T[d x 16 keys] . P^T[16 keys x 16 rows]
+  // so Q (the B operand of S^T) stays in registers for the whole item, K
+  // and V are read once per slot with ldmatrix (V transposed by ldmatrix
+  // itself), and P^T is S^T's accumulator moved across lanes by movmatrix.
+  // Rows are the item's 16 GQA-packed query rows, two n-tiles of 8; an item
+  // with at most 8 rows runs the first n-tile only.
+  //
+  // Lane (gid, tig) holds, per n-tile j, rows 8j+2tig and 8j+2tig+1; of
+  // S^T, keys gid and gid+8 of the slot; of O^T, two head-dim columns per
+  // 16-column tile:  16-bit caches 16mt+gid and 16mt+8+gid, E5M2 caches
+  // 16mt+2gid and 16mt+2gid+1.
+  //
+  // For E5M2 K, one 32-bit word of a key row holds four codes; widened they
+  // are two binary16 pairs, so within each 16-wide reduction step the lane's
+  // operand slots (2tig, 2tig+1 | 2tig+8, 2tig+9) hold head-dim columns
+  // 4tig .. 4tig+3, and Q's fragments are loaded with the same order.
   uint32_t phase = 0;  // bit s: parity of ring slot s
   int it_id = -1;
   Item f{};
-  int last[2] = {-1, -1};
-  float o[D / 8][4];
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  bool two = false;                  // the item has a second n-tile of rows
+  uint32_t qf[KSTEPS][2][2];         // Q^T fragments, per step and n-tile
+  float o[2][MT][4];                 // O^T accumulators
+  float m_use[2][2], l_run[2][2];    // per row: exponent reference, partial sum
+  int last[2][2];                    // per row: last visible key, -1 for padding
   const float sl2 = p.sl2;
+  const int key_lane = lane & 15, seg_lane = lane >> 4;
   for (int s = 0;; s = (s + 1 == NS ? 0 : s + 1)) {
     // refill the slot consumed by the previous iteration (at the start: the
     // one slot the prologue left empty), NS-1 slots ahead of this one
@@ -241,29 +257,39 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     const int chunk = mt.y & 0xFFFF;
     const bool bad = (mt.y >> 30) & 1;
     if (mt.x != it_id) {
-      // a new item: its rows' queries into the Q tile, fresh state
+      // a new item: its rows' Q fragments, fresh state
       it_id = mt.x;
       item_info(a, it_id, n_mblk, f);
-      for (int e = lane; e < 16 * (D / 8); e += 32) {
-        const int r = e / (D / 8), c8 = e % (D / 8);
-        const int R = f.r0 + r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (R < f.M) {
-          const T* src = static_cast<const T*>(a.q) +
-                         ((int64_t)(f.qs + R / p.g) * p.hq + f.kh * p.g + R % p.g) * D + c8 * 8;
-          v = __ldg(reinterpret_cast<const uint4*>(src));
+      two = f.M - f.r0 > 8;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int R = f.r0 + 8 * j + gid;
+        const T* qrow = static_cast<const T*>(a.q) +
+                        ((int64_t)(f.qs + R / p.g) * p.hq + f.kh * p.g + R % p.g) * D;
+        const bool ok = R < f.M;
+#pragma unroll
+        for (int kd = 0; kd < KSTEPS; ++kd) {
+          if constexpr (KV8) {
+            const uint2 v = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kd + 4 * tig))
+                               : make_uint2(0u, 0u);
+            qf[kd][j][0] = v.x;
+            qf[kd][j][1] = v.y;
+          } else {
+            const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kd + 2 * tig);
+            qf[kd][j][0] = ok ? __ldg(q32) : 0u;
+            qf[kd][j][1] = ok ? __ldg(q32 + 4) : 0u;
+          }
         }
-        st_shared_v4(sQ + (KV8 ? qswz8<D>(r, c8 * 8) : swz16(r, c8 * 8)), v);
-      }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int R = f.r0 + gid + 8 * h;
-        last[h] = R < f.M ? f.L - f.qb + R / p.g : -1;
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
-      }
+        for (int e = 0; e < 2; ++e) {
+          const int Rr = f.r0 + 8 * j + 2 * tig + e;
+          last[j][e] = Rr < f.M ? f.L - f.qb + Rr / p.g : -1;
+          m_use[j][e] = -INFINITY;
+          l_run[j][e] = 0.f;
+        }
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        for (int m = 0; m < MT; ++m) o[j][m][0] = o[j][m][1] = o[j][m][2] = o[j][m][3] = 0.f;
+      }
     }
     const uint32_t sK = wring + s * C::SLOT, sV = sK + C::HALF;
     const int kb = f.k0 + 16 * chunk;
@@ -271,133 +297,178 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
     if (nvalid < 16) {
       // keys past the row's end (or behind a bad table entry): zero their
       // K and V rows so stale or poisoned bytes never reach the products
-      constexpr int PIECES = D * C::ELT / 16;  // 16-byte pieces per key row
-      for (int e = lane; e < (16 - nvalid) * 2 * PIECES; e += 32) {
+      for (int e = lane; e < (16 - nvalid) * 2 * C::SEGS; e += 32) {
         const int kv = e & 1, rest = e >> 1;
-        const int r = nvalid + rest / PIECES, pc = rest % PIECES;
-        const uint32_t off = KV8 ? swz8(r, pc * 16) : swz16(r, pc * 8);
-        st_shared_v4((kv ? sV : sK) + off, make_uint4(0u, 0u, 0u, 0u));
-      }
-    }
-    __syncwarp();
-    uint32_t sVf = sV;  // 16-bit V tile the PV fragments come from
-    if (KV8) {
-      // widen this slot's V codes into the 16-bit staging tile
-      for (int e = lane; e < 16 * (D / 16); e += 32) {
-        const int r = e & 15, pc = e >> 4;  // 8 lanes of a quarter-warp: 8 rows, one piece
-        const uint4 w = ld_shared_v4(sV + swz8(r, pc * 16));
-        uint4 lo, hi;
-        e5m2x4_to<T>(w.x, lo.x, lo.y);
-        e5m2x4_to<T>(w.y, lo.z, lo.w);
-        e5m2x4_to<T>(w.z, hi.x, hi.y);
-        e5m2x4_to<T>(w.w, hi.z, hi.w);
-        st_shared_v4(sStg + swz16(r, pc * 16), lo);
-        st_shared_v4(sStg + swz16(r, pc * 16 + 8), hi);
+        const int r = nvalid + rest / C::SEGS, sg = rest % C::SEGS;
+        st_shared_v4((kv ? sV : sK) + seg_off(r, sg), make_uint4(0u, 0u, 0u, 0u));
       }
       __syncwarp();
-      sVf = sStg;
     }
 
-    // S = Q K^T: 16 rows x 16 keys
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S^T = K Q^T.  ldmatrix x4 at segments (sb, sb+1): lanes 0-15 address
+    // key rows 0-15 of segment sb, lanes 16-31 of segment sb+1.  Two
+    // accumulator sets shorten the dependent MMA chain.
+    float sa[2][2][4];
 #pragma unroll
-    for (int kd = 0; kd < D / 16; ++kd) {
-      uint32_t af[4], b0, b1, b2, b3;
-      if (KV8) {
-        // reduction index permuted within each 16-wide step: operand slots
-        // (2t, 2t+1 | 2t+8, 2t+9) hold head-dim columns 4t .. 4t+3
-        const uint2 q0 = ld_shared_v2(sQ + qswz8<D>(gid, kd * 16 + 4 * tig));
-        const uint2 q1 = ld_shared_v2(sQ + qswz8<D>(gid + 8, kd * 16 + 4 * tig));
-        af[0] = q0.x;
-        af[1] = q1.x;
-        af[2] = q0.y;
-        af[3] = q1.y;
-        e5m2x4_to<T>(ld_shared_u32(sK + swz8(gid, kd * 16 + 4 * tig)), b0, b1);
-        e5m2x4_to<T>(ld_shared_u32(sK + swz8(gid + 8, kd * 16 + 4 * tig)), b2, b3);
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) sa[u][j][0] = sa[u][j][1] = sa[u][j][2] = sa[u][j][3] = 0.f;
+#pragma unroll
+    for (int sb = 0; sb < C::SEGS; sb += 2) {
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4(sK + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
+      if constexpr (KV8) {
+        // r0/r1: keys gid/gid+8 of segment sb, r2/r3 of sb+1: two steps
+        uint32_t a0[4], a1[4];
+        e5m2x4_to<T>(r0, a0[0], a0[2]);
+        e5m2x4_to<T>(r1, a0[1], a0[3]);
+        e5m2x4_to<T>(r2, a1[0], a1[2]);
+        e5m2x4_to<T>(r3, a1[1], a1[3]);
+        const int kd = sb;
+        mma16816<T>(sa[0][0], a0, qf[kd][0][0], qf[kd][0][1]);
+        mma16816<T>(sa[1][0], a1, qf[kd + 1][0][0], qf[kd + 1][0][1]);
+        if (two) {
+          mma16816<T>(sa[0][1], a0, qf[kd][1][0], qf[kd][1][1]);
+          mma16816<T>(sa[1][1], a1, qf[kd + 1][1][0], qf[kd + 1][1][1]);
+        }
       } else {
-        ldsm_x4(sQ + swz16(lane & 15, kd * 16 + (lane >> 4) * 8), af[0], af[1], af[2], af[3]);
-        ldsm_x4(sK + swz16((lane & 7) + ((lane >> 4) << 3), kd * 16 + ((lane >> 3) & 1) * 8), b0,
-                b1, b2, b3);
-      }
-      mma16816<T>(sc[0], af, b0, b1);
-      mma16816<T>(sc[1], af, b2, b3);
-    }
-    // mask, online softmax (log2 units)
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int h = e >> 1;
-        const int j = kb + n * 8 + 2 * tig + (e & 1);
-        const float x = j <= last[h] ? sc[n][e] * sl2 : -INFINITY;
-        sc[n][e] = x;
-        mx[h] = fmaxf(mx[h], x);
+        // one step: head-dim columns 8*sb .. 8*sb+15
+        const uint32_t af[4] = {r0, r1, r2, r3};
+        const int kd = sb >> 1, u = kd & 1;
+        mma16816<T>(sa[u][0], af, qf[kd][0][0], qf[kd][0][1]);
+        if (two) mma16816<T>(sa[u][1], af, qf[kd][1][0], qf[kd][1][1]);
       }
     }
-    float alpha[2], m_use[2];
+    // sc[j][e + 2h] = logit of row 8j+2tig+e, key kb+gid+8h (log2 units, masked)
+    float sc[2][4];
+    bool need = false;
+    float mx[2][2];
+    mx[1][0] = mx[1][1] = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-      const float m_new = fmaxf(m_run[h], mx[h]);
-      m_use[h] = m_new == -INFINITY ? 0.f : m_new;
-      alpha[h] = exp2f(m_run[h] - m_use[h]);
-      m_run[h] = m_new;
-    }
-    float rs[2] = {0.f, 0.f};
+    for (int j = 0; j < 2; ++j) {
+      if (j == 1 && !two) break;
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
+      for (int e = 0; e < 2; ++e) {
+        float m = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = exp2f(sc[n][e] - m_use[e >> 1]);
-        sc[n][e] = pv;
-        rs[e >> 1] += pv;
+        for (int h = 0; h < 2; ++h) {
+          const int c = e + 2 * h;
+          const float x = kb + gid + 8 * h <= last[j][e] ? (sa[0][j][c] + sa[1][j][c]) * sl2
+                                                          : -INFINITY;
+          sc[j][c] = x;
+          m = fmaxf(m, x);
+        }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        mx[j][e] = m;
+        need |= m > m_use[j][e] + 8.f;
       }
     }
+    // lazy rescale: the exponent reference of a row moves only when the
+    // row's maximum passes it by more than 8 (a factor of 256), so
+    // p = 2^(x - ref) <= 256 and O^T is rescaled rarely.  The decision
+    // depends on the row's own logits only.
+    if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) l_run[h] = l_run[h] * alpha[h] + rs[h];
+      for (int j = 0; j < 2; ++j) {
+        if (j == 1 && !two) break;
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
+        for (int e = 0; e < 2; ++e) {
+          float alpha = 1.f;
+          if (mx[j][e] > m_use[j][e] + 8.f) {
+            alpha = exp2f(m_use[j][e] - mx[j][e]);
+            m_use[j][e] = mx[j][e];
+          }
+          l_run[j][e] *= alpha;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            o[j][m][e] *= alpha;
+            o[j][m][e + 2] *= alpha;
+          }
+        }
+      }
     }
-    // O += P V
-    uint32_t pf[4];
-    pf[0] = pack2<T>(sc[0][0], sc[0][1]);
-    pf[1] = pack2<T>(sc[0][2], sc[0][3]);
-    pf[2] = pack2<T>(sc[1][0], sc[1][1]);
-    pf[3] = pack2<T>(sc[1][2], sc[1][3]);
+    // P^T fragments: pack S^T's (row pair, key) values, transpose with movmatrix
+    uint32_t pb[2][2] = {{0u, 0u}, {0u, 0u}};
 #pragma unroll
-    for (int nd = 0; nd < D / 16; ++nd) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sVf + swz16((lane & 7) + (((lane >> 3) & 1) << 3), nd * 16 + (lane >> 4) * 8), b0,
-                b1, b2, b3);
-      mma16816<T>(o[2 * nd], pf, b0, b1);
-      mma16816<T>(o[2 * nd + 1], pf, b2, b3);
+    for (int j = 0; j < 2; ++j) {
+      if (j == 1 && !two) break;
+      float pv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float ref = m_use[j][c & 1] == -INFINITY ? 0.f : m_use[j][c & 1];
+        pv[c] = exp2f(sc[j][c] - ref);
+        l_run[j][c & 1] += pv[c];
+      }
+      pb[j][0] = movm_t(pack2<T>(pv[0], pv[1]));  // keys 2tig, 2tig+1 of row gid
+      pb[j][1] = movm_t(pack2<T>(pv[2], pv[3]));  // keys 8+2tig, 9+2tig
+    }
+
+    // O^T += V^T P^T
+    if constexpr (KV8) {
+      // ldmatrix.trans on the codes as 16-bit pairs: lane (gid, tig) gets
+      // keys 2tig, 2tig+1 of head-dim columns 2gid, 2gid+1 of a segment; one
+      // byte permute per operand register places each code in the high byte
+      // of a binary16 (the exact E5M2 -> binary16 widening).
+#pragma unroll
+      for (int sb = 0; sb < C::SEGS; sb += 2) {
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4_t(sV + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
+        const uint32_t aa[4] = {h2_to<T>(__byte_perm(r0, 0u, 0x2404)),
+                                h2_to<T>(__byte_perm(r0, 0u, 0x3414)),
+                                h2_to<T>(__byte_perm(r1, 0u, 0x2404)),
+                                h2_to<T>(__byte_perm(r1, 0u, 0x3414))};
+        const uint32_t ab[4] = {h2_to<T>(__byte_perm(r2, 0u, 0x2404)),
+                                h2_to<T>(__byte_perm(r2, 0u, 0x3414)),
+                                h2_to<T>(__byte_perm(r3, 0u, 0x2404)),
+                                h2_to<T>(__byte_perm(r3, 0u, 0x3414))};
+        mma16816<T>(o[0][sb], aa, pb[0][0], pb[0][1]);
+        mma16816<T>(o[0][sb + 1], ab, pb[0][0], pb[0][1]);
+        if (two) {
+          mma16816<T>(o[1][sb], aa, pb[1][0], pb[1][1]);
+          mma16816<T>(o[1][sb + 1], ab, pb[1][0], pb[1][1]);
+        }
+      }
+    } else {
+      // x4.trans: keys 0-7 / 8-15 (lane bit 4) of segments 2mt / 2mt+1 (lane bit 3)
+      const int vkey = (lane & 7) + ((lane >> 4) << 3), vseg = (lane >> 3) & 1;
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        uint32_t af[4];
+        ldsm_x4_t(sV + seg_off(vkey, 2 * m + vseg), af[0], af[1], af[2], af[3]);
+        mma16816<T>(o[0][m], af, pb[0][0], pb[0][1]);
+        if (two) mma16816<T>(o[1][m], af, pb[1][0], pb[1][1]);
+      }
     }
 
     if (chunk == f.nchunks - 1) {
       // item done: this split's partial state of the block's rows
-      float lt[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        lt[h] = l_run[h] + __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-        lt[h] += __shfl_xor_sync(0xffffffffu, lt[h], 2);
-      }
+      for (int j = 0; j < 2; ++j) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int R = f.r0 + gid + 8 * h;
-        if (R >= f.M) continue;
-        const int64_t slot = f.slot_base + R / p.g;
-        const int64_t ps = (slot * p.hq + f.kh * p.g + R % p.g) * NSPLIT + f.split;
-        float* acc = a.part_acc + ps * D;
+        for (int e = 0; e < 2; ++e) {
+          float lt = l_run[j][e];
+          lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+          lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+          lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+          const int R = f.r0 + 8 * j + 2 * tig + e;
+          if (R >= f.M) continue;
+          const int64_t slot = f.slot_base + R / p.g;
+          const int64_t ps = (slot * p.hq + f.kh * p.g + R % p.g) * NSPLIT + f.split;
+          float* acc = a.part_acc + ps * D;
 #pragma unroll
-        for (int n = 0; n < D / 8; ++n)
-          *reinterpret_cast<float2*>(acc + n * 8 + 2 * tig) = make_float2(o[n][2 * h], o[n][2 * h + 1]);
-        if (tig == 0) a.part_ml[ps] = make_float2(m_run[h], lt[h]);
+          for (int m = 0; m < MT; ++m) {
+            if constexpr (KV8) {
+              *reinterpret_cast<float2*>(acc + 16 * m + 2 * gid) =
+                  make_float2(o[j][m][e], o[j][m][e + 2]);
+            } else {
+              acc[16 * m + gid] = o[j][m][e];
+              acc[16 * m + 8 + gid] = o[j][m][e + 2];
+            }
+          }
+          if (gid == 0) a.part_ml[ps] = make_float2(m_use[j][e], lt);
+        }
       }
     }
     // the slot is consumed; the next iteration refills it with TMA (async
@@ -416,7 +487,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1)
   if (lane == 0) {
     __threadfence();
     const uint32_t done = atomicAdd(counters + 1, 1u);
-    if (done == gridDim.x * DEC_WARPS - 1) {
+    if (done == gridDim.x * C::W - 1) {
       counters[0] = 0u;
       counters[1] = 0u;
       __threadfence();
@@ -438,9 +509,9 @@ cudaError_t launch_dec(const AttnArgs& a, const CUtensorMap& tk, const CUtensorM
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int grid = sms > 0 ? sms : 148;  // persistent: one CTA per SM
-  if (total_items < grid * DEC_WARPS) grid = (total_items + DEC_WARPS - 1) / DEC_WARPS;
+  if (total_items < grid * C::W) grid = (total_items + C::W - 1) / C::W;
   if (grid < 1) grid = 1;
-  k<<<grid, DEC_WARPS * 32, C::SMEM, st>>>(a, tk, tv, total_items, n_mblk, counters);
+  k<<<grid, C::W * 32, C::SMEM, st>>>(a, tk, tv, total_items, n_mblk, counters);
   return cudaGetLastError();
 }
 
