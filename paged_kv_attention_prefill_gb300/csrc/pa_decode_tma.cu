@@ -38,6 +38,8 @@
 // which warp ran it or when, so the outputs stay bitwise batch-invariant.
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "pa_sm100.cuh"
 
 namespace pa {
@@ -57,14 +59,36 @@ struct DecCfg {
   static constexpr uint32_t SLOT = 2 * HALF;
   static constexpr int W = SLOT >= 16384 ? 4 : 8;          // warps per CTA, one ring each
   static constexpr int NS_FIT = (224 * 1024) / (W * SLOT);
-  static constexpr int NS = NS_FIT < 16 ? NS_FIT : 16;     // ring slots per warp
+  static constexpr int G = NS_FIT >= 6 ? 2 : 1;            // slots consumed per iteration
+  static constexpr int NS = (NS_FIT < 16 ? NS_FIT : 16) / G * G;  // ring slots per warp
   static constexpr uint32_t OFF_BAR = W * NS * SLOT;       // all rings first (1 KB aligned)
   static constexpr uint32_t OFF_META = OFF_BAR + W * NS * 8;
   static constexpr uint32_t SMEM = OFF_META + W * NS * 8 + 1024;
   static_assert(SLOT % 1024 == 0, "slot alignment");
-  static_assert(NS >= 3, "ring depth");
+  static_assert(NS >= 2 * G && NS % G == 0 && NS <= 32, "ring depth");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
+
+constexpr int META_BAD = 1 << 30;  // block-table entry out of range: no copy
+constexpr int META_PAD = 1 << 29;  // padding slot of an item: no copy
+
+// Waits for the phase with the given parity; every lane polls, lane 0 alone
+// decides to give up (after WAIT_LIMIT_CYCLES), so the warp leaves together.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int lane,
+                                               uint32_t* err) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((it & 63u) == 63u) {
+      const int late = __shfl_sync(0xffffffffu, (int)(clock64() - t0 > WAIT_LIMIT_CYCLES), 0);
+      if (late) {
+        if (lane == 0) atomicOr(err, PA_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
 
 // Byte offset of 16-byte segment `seg` of key row `key` (0..15) in a slot
 // half: [segs / 8][16 rows][128 B] with the 128-byte swizzle the TMA boxes
@@ -159,7 +183,6 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   const uint32_t wring = base + warp * NS * C::SLOT;  // this warp's slots
   const uint32_t bar0 = base + C::OFF_BAR + warp * NS * 8;
   int2* meta = reinterpret_cast<int2*>(smem + C::OFF_META) + warp * NS;
-  volatile int abort_local = 0;  // a timed-out wait ends this warp's work
 
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -169,51 +192,86 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   }
   __syncwarp();
 
-  // ---- producer cursor (lane 0 only) --------------------------------------
-  int cur_id = -1, cur_chunk = 0;
+  // ---- producer (warp-uniform state; lane 0 issues the copies) -------------
+  // The cursor walks the item's 16-key slots, padded to a multiple of G.  The
+  // block-table entries come from two 32-entry windows held one per lane
+  // (the next window is loaded while the current one is in use), so a slot's
+  // page costs one shuffle instead of a dependent global load.
+  int cur_id = -1, cur_chunk = 0, cur_n = 0;
+  int pcol = 0, poff = 0, wbase = 0, win = -1, win_next = -1;
   Item cur{};
+  auto bt_entry = [&](int col) {
+    return col < p.max_pages ? __ldg(p.bt + (int64_t)cur.b * p.max_pages + col) : -1;
+  };
   auto fetch = [&]() {
-    // next non-empty item, or -1
+    // next non-empty item, or cur_id = -1
     for (;;) {
-      const int id = (int)atomicAdd(counters, 1u);
-      if (id >= total_items) return -1;
-      if (item_info(a, id, n_mblk, cur)) return id;
+      int id = 0;
+      if (lane == 0) id = (int)atomicAdd(counters, 1u);
+      id = __shfl_sync(0xffffffffu, id, 0);
+      if (id >= total_items) {
+        cur_id = -1;
+        return;
+      }
+      if (item_info(a, id, n_mblk, cur)) {
+        cur_id = id;
+        cur_chunk = 0;
+        cur_n = (cur.nchunks + C::G - 1) / C::G * C::G;
+        pcol = cur.k0 / p.page_size;
+        poff = cur.k0 % p.page_size;
+        wbase = pcol & ~31;
+        win = bt_entry(wbase + lane);
+        win_next = bt_entry(wbase + 32 + lane);
+        return;
+      }
     }
   };
   auto issue = [&](int s) {
-    // the cursor's next 16-key slot into ring slot s (or mark the end)
+    // the cursor's next slot into ring slot s (or mark the end)
+    const uint32_t bar = bar0 + 8 * s;
     if (cur_id < 0) {
-      meta[s] = make_int2(-1, 0);
+      if (lane == 0) meta[s] = make_int2(-1, 0);
       return;
     }
-    const int s0 = cur.k0 + 16 * cur_chunk;
-    const int col = s0 / p.page_size;
-    const int page = col < p.max_pages ? __ldg(p.bt + (int64_t)cur.b * p.max_pages + col) : -1;
-    const uint32_t bar = bar0 + 8 * s;
-    if (page < 0 || page >= p.num_pages) {
-      atomicOr(p.err, PA_DEVERR_BAD_PAGE);
-      meta[s] = make_int2(cur_id, cur_chunk | (1 << 30));  // the consumer zero-fills
-      mbar_arrive(bar);
+    if (cur_chunk >= cur.nchunks) {
+      if (lane == 0) {
+        meta[s] = make_int2(cur_id, cur_chunk | META_PAD);
+        mbar_arrive(bar);
+      }
     } else {
-      const int tok0 = page * p.page_size + (s0 % p.page_size);
-      meta[s] = make_int2(cur_id, cur_chunk);
-      mbar_arrive_expect_tx(bar, C::SLOT);
-      const uint32_t dK = wring + s * C::SLOT, dV = dK + C::HALF;
+      if (pcol >= wbase + 32) {  // pages advance at most one column per slot
+        wbase += 32;
+        win = win_next;
+        win_next = bt_entry(wbase + 32 + lane);
+      }
+      const int page = __shfl_sync(0xffffffffu, win, pcol - wbase);
+      if (lane == 0) {
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+          meta[s] = make_int2(cur_id, cur_chunk | META_BAD);
+          mbar_arrive(bar);
+        } else {
+          const int tok0 = page * p.page_size + poff;
+          meta[s] = make_int2(cur_id, cur_chunk);
+          mbar_arrive_expect_tx(bar, C::SLOT);
+          const uint32_t dK = wring + s * C::SLOT, dV = dK + C::HALF;
 #pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(dK + c * 2048, &tmK, c * (128 / C::ELT), cur.kh, tok0, bar);
-        tma_load_3d(dV + c * 2048, &tmV, c * (128 / C::ELT), cur.kh, tok0, bar);
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_load_3d(dK + c * 2048, &tmK, c * (128 / C::ELT), cur.kh, tok0, bar);
+            tma_load_3d(dV + c * 2048, &tmV, c * (128 / C::ELT), cur.kh, tok0, bar);
+          }
+        }
+      }
+      poff += 16;
+      if (poff >= p.page_size) {
+        poff -= p.page_size;
+        ++pcol;
       }
     }
-    if (++cur_chunk >= cur.nchunks) {
-      cur_chunk = 0;
-      cur_id = fetch();
-    }
+    if (++cur_chunk >= cur_n) fetch();
   };
-  if (lane == 0) {
-    cur_id = fetch();
-    for (int s = 0; s < NS - 1; ++s) issue(s);
-  }
+  fetch();
+  for (int s = 0; s < NS - C::G; ++s) issue(s);
   __syncwarp();
 
   // ---- consumer -------------------------------------------------------------
@@ -224,10 +282,13 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   // and V are read once per slot with ldmatrix (V transposed by ldmatrix
   // itself), and P^T is S^T's accumulator moved across lanes by movmatrix.
   // Rows are the item's 16 GQA-packed query rows, two n-tiles of 8; an item
-  // with at most 8 rows runs the first n-tile only.
+  // with at most 8 rows runs the first n-tile only.  Each iteration takes G
+  // consecutive ring slots of one item (items are padded to a multiple of
+  // G), which gives the dependent MMA chains G-fold independence and shares
+  // the softmax reductions.
   //
   // Lane (gid, tig) holds, per n-tile j, rows 8j+2tig and 8j+2tig+1; of
-  // S^T, keys gid and gid+8 of the slot; of O^T, two head-dim columns per
+  // S^T, keys gid and gid+8 of each slot; of O^T, two head-dim columns per
   // 16-column tile:  16-bit caches 16mt+gid and 16mt+8+gid, E5M2 caches
   // 16mt+2gid and 16mt+2gid+1.
   //
@@ -235,7 +296,10 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   // are two binary16 pairs, so within each 16-wide reduction step the lane's
   // operand slots (2tig, 2tig+1 | 2tig+8, 2tig+9) hold head-dim columns
   // 4tig .. 4tig+3, and Q's fragments are loaded with the same order.
-  uint32_t phase = 0;  // bit s: parity of ring slot s
+  constexpr int G = C::G;
+  constexpr int NACC = G == 1 && D <= 128 ? 2 : 1;  // accumulator sets per slot for S^T
+  uint32_t phase = 0;                   // bit s: parity of ring slot s
+  bool aborted = false;
   int it_id = -1;
   Item f{};
   bool two = false;                  // the item has a second n-tile of rows
@@ -245,20 +309,30 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   int last[2][2];                    // per row: last visible key, -1 for padding
   const float sl2 = p.sl2;
   const int key_lane = lane & 15, seg_lane = lane >> 4;
-  for (int s = 0;; s = (s + 1 == NS ? 0 : s + 1)) {
-    // refill the slot consumed by the previous iteration (at the start: the
-    // one slot the prologue left empty), NS-1 slots ahead of this one
-    if (lane == 0) issue(s == 0 ? NS - 1 : s - 1);
+  for (int s = 0;; s = (s + G == NS ? 0 : s + G)) {
+    // refill the group consumed by the previous iteration (at the start: the
+    // one group the prologue left empty), NS-G slots ahead of this group
+    {
+      const int r = s == 0 ? NS - G : s - G;
+#pragma unroll
+      for (int u = 0; u < G; ++u) issue(r + u);
+    }
     __syncwarp();
-    const int2 mt = meta[s];
-    if (mt.x < 0) break;
-    if (!mbar_wait(bar0 + 8 * s, (phase >> s) & 1u, &abort_local, p.err)) break;
-    phase ^= 1u << s;
-    const int chunk = mt.y & 0xFFFF;
-    const bool bad = (mt.y >> 30) & 1;
-    if (mt.x != it_id) {
+    const int2 mt0 = meta[s];
+    if (mt0.x < 0) break;
+    bool ok = true;
+#pragma unroll
+    for (int u = 0; u < G; ++u)
+      ok = ok && mbar_wait_warp(bar0 + 8 * (s + u), (phase >> (s + u)) & 1u, lane, p.err);
+    if (!ok) {
+      aborted = true;
+      break;
+    }
+#pragma unroll
+    for (int u = 0; u < G; ++u) phase ^= 1u << (s + u);
+    if (mt0.x != it_id) {
       // a new item: its rows' Q fragments, fresh state
-      it_id = mt.x;
+      it_id = mt0.x;
       item_info(a, it_id, n_mblk, f);
       two = f.M - f.r0 > 8;
 #pragma unroll
@@ -266,18 +340,18 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
         const int R = f.r0 + 8 * j + gid;
         const T* qrow = static_cast<const T*>(a.q) +
                         ((int64_t)(f.qs + R / p.g) * p.hq + f.kh * p.g + R % p.g) * D;
-        const bool ok = R < f.M;
+        const bool qok = R < f.M;
 #pragma unroll
         for (int kd = 0; kd < KSTEPS; ++kd) {
           if constexpr (KV8) {
-            const uint2 v = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kd + 4 * tig))
-                               : make_uint2(0u, 0u);
+            const uint2 v = qok ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * kd + 4 * tig))
+                                : make_uint2(0u, 0u);
             qf[kd][j][0] = v.x;
             qf[kd][j][1] = v.y;
           } else {
             const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qrow + 16 * kd + 2 * tig);
-            qf[kd][j][0] = ok ? __ldg(q32) : 0u;
-            qf[kd][j][1] = ok ? __ldg(q32 + 4) : 0u;
+            qf[kd][j][0] = qok ? __ldg(q32) : 0u;
+            qf[kd][j][1] = qok ? __ldg(q32 + 4) : 0u;
           }
         }
 #pragma unroll
@@ -291,158 +365,187 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
         for (int m = 0; m < MT; ++m) o[j][m][0] = o[j][m][1] = o[j][m][2] = o[j][m][3] = 0.f;
       }
     }
-    const uint32_t sK = wring + s * C::SLOT, sV = sK + C::HALF;
-    const int kb = f.k0 + 16 * chunk;
-    const int nvalid = bad ? 0 : min(16, f.L - kb);
-    if (nvalid < 16) {
-      // keys past the row's end (or behind a bad table entry): zero their
-      // K and V rows so stale or poisoned bytes never reach the products
-      for (int e = lane; e < (16 - nvalid) * 2 * C::SEGS; e += 32) {
-        const int kv = e & 1, rest = e >> 1;
-        const int r = nvalid + rest / C::SEGS, sg = rest % C::SEGS;
-        st_shared_v4((kv ? sV : sK) + seg_off(r, sg), make_uint4(0u, 0u, 0u, 0u));
+    const int chunk0 = mt0.y & 0xFFFF;
+    int kb[G], nvalid[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const int my = meta[s + u].y;
+      kb[u] = f.k0 + 16 * (chunk0 + u);
+      nvalid[u] = (my & (META_BAD | META_PAD)) ? 0 : min(16, f.L - kb[u]);
+      if (nvalid[u] < 16) {
+        // keys past the row's end, padding slots and slots behind a bad
+        // table entry: zero their V rows so stale or poisoned bytes never
+        // reach P V (their logits are masked, whatever K holds)
+        const uint32_t sV = wring + (s + u) * C::SLOT + C::HALF;
+        for (int e = lane; e < (16 - nvalid[u]) * C::SEGS; e += 32)
+          st_shared_v4(sV + seg_off(nvalid[u] + e / C::SEGS, e % C::SEGS),
+                       make_uint4(0u, 0u, 0u, 0u));
+        __syncwarp();
       }
-      __syncwarp();
     }
 
-    // S^T = K Q^T.  ldmatrix x4 at segments (sb, sb+1): lanes 0-15 address
-    // key rows 0-15 of segment sb, lanes 16-31 of segment sb+1.  Two
-    // accumulator sets shorten the dependent MMA chain.
-    float sa[2][2][4];
+    // The slot math, compiled once per count of 8-row n-tiles so that the
+    // unrolled MMA sequences carry no branches.
+    auto math = [&](auto nt_const) {
+      constexpr int NT = decltype(nt_const)::value;
+      // S^T = K Q^T.  ldmatrix x4 at segments (sb, sb+1): lanes 0-15 address
+      // key rows 0-15 of segment sb, lanes 16-31 of segment sb+1.
+      float sa[G][NACC][NT][4];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < G; ++u)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) sa[u][j][0] = sa[u][j][1] = sa[u][j][2] = sa[u][j][3] = 0.f;
+        for (int c = 0; c < NACC; ++c)
 #pragma unroll
-    for (int sb = 0; sb < C::SEGS; sb += 2) {
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4(sK + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
-      if constexpr (KV8) {
-        // r0/r1: keys gid/gid+8 of segment sb, r2/r3 of sb+1: two steps
-        uint32_t a0[4], a1[4];
-        e5m2x4_to<T>(r0, a0[0], a0[2]);
-        e5m2x4_to<T>(r1, a0[1], a0[3]);
-        e5m2x4_to<T>(r2, a1[0], a1[2]);
-        e5m2x4_to<T>(r3, a1[1], a1[3]);
-        const int kd = sb;
-        mma16816<T>(sa[0][0], a0, qf[kd][0][0], qf[kd][0][1]);
-        mma16816<T>(sa[1][0], a1, qf[kd + 1][0][0], qf[kd + 1][0][1]);
-        if (two) {
-          mma16816<T>(sa[0][1], a0, qf[kd][1][0], qf[kd][1][1]);
-          mma16816<T>(sa[1][1], a1, qf[kd + 1][1][0], qf[kd + 1][1][1]);
-        }
-      } else {
-        // one step: head-dim columns 8*sb .. 8*sb+15
-        const uint32_t af[4] = {r0, r1, r2, r3};
-        const int kd = sb >> 1, u = kd & 1;
-        mma16816<T>(sa[u][0], af, qf[kd][0][0], qf[kd][0][1]);
-        if (two) mma16816<T>(sa[u][1], af, qf[kd][1][0], qf[kd][1][1]);
-      }
-    }
-    // sc[j][e + 2h] = logit of row 8j+2tig+e, key kb+gid+8h (log2 units, masked)
-    float sc[2][4];
-    bool need = false;
-    float mx[2][2];
-    mx[1][0] = mx[1][1] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j == 1 && !two) break;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = e + 2 * h;
-          const float x = kb + gid + 8 * h <= last[j][e] ? (sa[0][j][c] + sa[1][j][c]) * sl2
-                                                          : -INFINITY;
-          sc[j][c] = x;
-          m = fmaxf(m, x);
-        }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        mx[j][e] = m;
-        need |= m > m_use[j][e] + 8.f;
-      }
-    }
-    // lazy rescale: the exponent reference of a row moves only when the
-    // row's maximum passes it by more than 8 (a factor of 256), so
-    // p = 2^(x - ref) <= 256 and O^T is rescaled rarely.  The decision
-    // depends on the row's own logits only.
-    if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        if (j == 1 && !two) break;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float alpha = 1.f;
-          if (mx[j][e] > m_use[j][e] + 8.f) {
-            alpha = exp2f(m_use[j][e] - mx[j][e]);
-            m_use[j][e] = mx[j][e];
-          }
-          l_run[j][e] *= alpha;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            o[j][m][e] *= alpha;
-            o[j][m][e + 2] *= alpha;
-          }
-        }
-      }
-    }
-    // P^T fragments: pack S^T's (row pair, key) values, transpose with movmatrix
-    uint32_t pb[2][2] = {{0u, 0u}, {0u, 0u}};
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (j == 1 && !two) break;
-      float pv[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float ref = m_use[j][c & 1] == -INFINITY ? 0.f : m_use[j][c & 1];
-        pv[c] = exp2f(sc[j][c] - ref);
-        l_run[j][c & 1] += pv[c];
-      }
-      pb[j][0] = movm_t(pack2<T>(pv[0], pv[1]));  // keys 2tig, 2tig+1 of row gid
-      pb[j][1] = movm_t(pack2<T>(pv[2], pv[3]));  // keys 8+2tig, 9+2tig
-    }
-
-    // O^T += V^T P^T
-    if constexpr (KV8) {
-      // ldmatrix.trans on the codes as 16-bit pairs: lane (gid, tig) gets
-      // keys 2tig, 2tig+1 of head-dim columns 2gid, 2gid+1 of a segment; one
-      // byte permute per operand register places each code in the high byte
-      // of a binary16 (the exact E5M2 -> binary16 widening).
+          for (int j = 0; j < NT; ++j)
+            sa[u][c][j][0] = sa[u][c][j][1] = sa[u][c][j][2] = sa[u][c][j][3] = 0.f;
 #pragma unroll
       for (int sb = 0; sb < C::SEGS; sb += 2) {
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_t(sV + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
-        const uint32_t aa[4] = {h2_to<T>(__byte_perm(r0, 0u, 0x2404)),
-                                h2_to<T>(__byte_perm(r0, 0u, 0x3414)),
-                                h2_to<T>(__byte_perm(r1, 0u, 0x2404)),
-                                h2_to<T>(__byte_perm(r1, 0u, 0x3414))};
-        const uint32_t ab[4] = {h2_to<T>(__byte_perm(r2, 0u, 0x2404)),
-                                h2_to<T>(__byte_perm(r2, 0u, 0x3414)),
-                                h2_to<T>(__byte_perm(r3, 0u, 0x2404)),
-                                h2_to<T>(__byte_perm(r3, 0u, 0x3414))};
-        mma16816<T>(o[0][sb], aa, pb[0][0], pb[0][1]);
-        mma16816<T>(o[0][sb + 1], ab, pb[0][0], pb[0][1]);
-        if (two) {
-          mma16816<T>(o[1][sb], aa, pb[1][0], pb[1][1]);
-          mma16816<T>(o[1][sb + 1], ab, pb[1][0], pb[1][1]);
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+          const uint32_t sK = wring + (s + u) * C::SLOT;
+          uint32_t r0, r1, r2, r3;
+          ldsm_x4(sK + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
+          if constexpr (KV8) {
+            // r0/r1: keys gid/gid+8 of segment sb, r2/r3 of sb+1: two steps
+            uint32_t a0[4], a1[4];
+            e5m2x4_to<T>(r0, a0[0], a0[2]);
+            e5m2x4_to<T>(r1, a0[1], a0[3]);
+            e5m2x4_to<T>(r2, a1[0], a1[2]);
+            e5m2x4_to<T>(r3, a1[1], a1[3]);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              mma16816<T>(sa[u][0][j], a0, qf[sb][j][0], qf[sb][j][1]);
+              mma16816<T>(sa[u][NACC - 1][j], a1, qf[sb + 1][j][0], qf[sb + 1][j][1]);
+            }
+          } else {
+            // one step: head-dim columns 8*sb .. 8*sb+15
+            const uint32_t af[4] = {r0, r1, r2, r3};
+            const int kd = sb >> 1, c = NACC == 1 ? 0 : (kd & 1);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma16816<T>(sa[u][c][j], af, qf[kd][j][0], qf[kd][j][1]);
+          }
         }
       }
-    } else {
-      // x4.trans: keys 0-7 / 8-15 (lane bit 4) of segments 2mt / 2mt+1 (lane bit 3)
-      const int vkey = (lane & 7) + ((lane >> 4) << 3), vseg = (lane >> 3) & 1;
+      // sc[u][j][e + 2h] = logit of row 8j+2tig+e, key kb[u]+gid+8h (log2
+      // units, masked), kept in sa[u][0]
+      bool need = false;
+      float mx[NT][2];
 #pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        uint32_t af[4];
-        ldsm_x4_t(sV + seg_off(vkey, 2 * m + vseg), af[0], af[1], af[2], af[3]);
-        mma16816<T>(o[0][m], af, pb[0][0], pb[0][1]);
-        if (two) mma16816<T>(o[1][m], af, pb[1][0], pb[1][1]);
+      for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < G; ++u) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = e + 2 * h;
+              float x = sa[u][0][j][c];
+              if (NACC == 2) x += sa[u][NACC - 1][j][c];
+              x = gid + 8 * h < nvalid[u] && kb[u] + gid + 8 * h <= last[j][e] ? x * sl2
+                                                                                : -INFINITY;
+              sa[u][0][j][c] = x;
+              m = fmaxf(m, x);
+            }
+          }
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          mx[j][e] = m;
+          need |= m > m_use[j][e] + 8.f;
+        }
       }
-    }
+      // lazy rescale: the exponent reference of a row moves only when the
+      // row's maximum passes it by more than 8 (a factor of 256), so
+      // p = 2^(x - ref) <= 256 and O^T is rescaled rarely.  The decision
+      // depends on the row's own logits only.
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float alpha = 1.f;
+            if (mx[j][e] > m_use[j][e] + 8.f) {
+              alpha = exp2f(m_use[j][e] - mx[j][e]);
+              m_use[j][e] = mx[j][e];
+            }
+            l_run[j][e] *= alpha;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              o[j][m][e] *= alpha;
+              o[j][m][e + 2] *= alpha;
+            }
+          }
+        }
+      }
+      // P^T fragments: pack S^T's (row pair, key) values, transpose with movmatrix
+      uint32_t pb[G][NT][2];
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float pv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float ref = m_use[j][c & 1] == -INFINITY ? 0.f : m_use[j][c & 1];
+            pv[c] = exp2f(sa[u][0][j][c] - ref);
+            l_run[j][c & 1] += pv[c];
+          }
+          pb[u][j][0] = movm_t(pack2<T>(pv[0], pv[1]));  // keys 2tig, 2tig+1 of row gid
+          pb[u][j][1] = movm_t(pack2<T>(pv[2], pv[3]));  // keys 8+2tig, 9+2tig
+        }
+      }
 
-    if (chunk == f.nchunks - 1) {
+      // O^T += V^T P^T
+      if constexpr (KV8) {
+        // ldmatrix.trans on the codes as 16-bit pairs: lane (gid, tig) gets
+        // keys 2tig, 2tig+1 of head-dim columns 2gid, 2gid+1 of a segment;
+        // one byte permute per operand register places each code in the
+        // high byte of a binary16 (the exact E5M2 -> binary16 widening).
+#pragma unroll
+        for (int sb = 0; sb < C::SEGS; sb += 2) {
+#pragma unroll
+          for (int u = 0; u < G; ++u) {
+            const uint32_t sV = wring + (s + u) * C::SLOT + C::HALF;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(sV + seg_off(key_lane, sb + seg_lane), r0, r1, r2, r3);
+            const uint32_t aa[4] = {h2_to<T>(__byte_perm(r0, 0u, 0x2404)),
+                                    h2_to<T>(__byte_perm(r0, 0u, 0x3414)),
+                                    h2_to<T>(__byte_perm(r1, 0u, 0x2404)),
+                                    h2_to<T>(__byte_perm(r1, 0u, 0x3414))};
+            const uint32_t ab[4] = {h2_to<T>(__byte_perm(r2, 0u, 0x2404)),
+                                    h2_to<T>(__byte_perm(r2, 0u, 0x3414)),
+                                    h2_to<T>(__byte_perm(r3, 0u, 0x2404)),
+                                    h2_to<T>(__byte_perm(r3, 0u, 0x3414))};
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              mma16816<T>(o[j][sb], aa, pb[u][j][0], pb[u][j][1]);
+              mma16816<T>(o[j][sb + 1], ab, pb[u][j][0], pb[u][j][1]);
+            }
+          }
+        }
+      } else {
+        // x4.trans: keys 0-7 / 8-15 (lane bit 4) of segments 2mt / 2mt+1 (lane bit 3)
+        const int vkey = (lane & 7) + ((lane >> 4) << 3), vseg = (lane >> 3) & 1;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+#pragma unroll
+          for (int u = 0; u < G; ++u) {
+            const uint32_t sV = wring + (s + u) * C::SLOT + C::HALF;
+            uint32_t af[4];
+            ldsm_x4_t(sV + seg_off(vkey, 2 * m + vseg), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) mma16816<T>(o[j][m], af, pb[u][j][0], pb[u][j][1]);
+          }
+        }
+      }
+    };
+    if (two)
+      math(std::integral_constant<int, 2>{});
+    else
+      math(std::integral_constant<int, 1>{});
+
+    if (chunk0 + G >= f.nchunks) {
       // item done: this split's partial state of the block's rows
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -471,14 +574,16 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
         }
       }
     }
-    // the slot is consumed; the next iteration refills it with TMA (async
+    // the group is consumed; the next iteration refills it with TMA (async
     // writes after this warp's generic reads and zero-fills)
     fence_proxy_async_smem();
     __syncwarp();
   }
 
-  // a timed-out warp may still have copies landing: let them finish
-  if (abort_local) {
+  // a timed-out warp may still have copies landing: let them finish (slots
+  // waited on successfully in the failed group still hold their old parity,
+  // so their drain returns at once)
+  if (aborted && lane == 0) {
     for (int s = 0; s < NS; ++s)
       if (meta[s].x >= 0) mbar_drain(bar0 + 8 * s, (phase >> s) & 1u, p.err);
   }
