@@ -21,6 +21,8 @@ WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_deco
   size_t off = sizeof(WsHeader);
   w.dec_base = off;
   off += align_up((size_t)num_rows * 4, 256);
+  w.row_order = off;
+  off += align_up((size_t)num_rows * 4, 256);
   w.slot_tok = off;
   off += align_up((size_t)w.max_slots * 4, 256);
   w.tiles = off;
@@ -177,11 +179,17 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.part_ml = reinterpret_cast<float2*>(base + w.part_ml);
   a.dec_base = nullptr;
   a.slot_tok = nullptr;
+  a.row_order = nullptr;
   a.tiles = reinterpret_cast<const int2*>(base + w.tiles);
   a.n_tiles = &reinterpret_cast<const WsHeader*>(base)->n_tiles;
   a.max_decode_q = r.max_dq;
   a.max_slots = w.max_slots;
   return a;
+}
+
+int32_t* row_order_of(void* ws, const pa_batch* bat, const Resolved& r) {
+  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g);
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + w.row_order);
 }
 
 inline pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
@@ -191,16 +199,26 @@ int decode_mblocks(const Resolved& r, int max_q) {
 }
 
 // Launches the decode CTAs and the merge for the rows routed to decode.
+// The persistent decode kernel takes its items in row order; listing the rows
+// with the longest splits first keeps the last items short, so fewer warps
+// idle at the end.  Small batches skip the extra launch.
+constexpr int ORDER_MIN_ROWS = 16;
+
 cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_slots,
-                       cudaStream_t st) {
+                       int32_t* order, cudaStream_t st) {
   AttnArgs a = a0;
   a.dec_mblk = n_mblk;
   cudaError_t e;
   if (r.qd == PA_F32)
     e = launch_f32(a, 1, 0, n_mblk, st);
-  else if (decode_tma_supported(r.qd, r.kvd, r.d, (int64_t)a.p.num_pages * a.p.page_size))
+  else if (decode_tma_supported(r.qd, r.kvd, r.d, (int64_t)a.p.num_pages * a.p.page_size)) {
+    if (order && a.p.num_rows >= ORDER_MIN_ROWS && a.p.num_rows <= MAX_ORDER_ROWS) {
+      e = launch_row_order(a, order, st);
+      if (e != cudaSuccess) return e;
+      a.row_order = order;
+    }
     e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, st);
-  else
+  } else
     e = launch_decode_mma(a, r.qd, r.kvd, n_mblk, st);
   if (e != cudaSuccess) return e;
   return launch_merge(a, r.qd, n_slots, st);
@@ -255,7 +273,8 @@ pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, cons
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
-  return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots, st));
+  return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots,
+                                row_order_of(workspace, batch, r), st));
 }
 
 pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const void* q,
@@ -280,7 +299,8 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = r.host ? r.host_slots : (int)a.max_slots;
   if (max_q > 0) {
-    e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, st);
+    e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(workspace, batch, r),
+                   st);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   const int grid = r.host ? r.host_tiles : max_tiles;
@@ -379,5 +399,6 @@ extern "C" pa_status paged_attn_decode_static(const pa_params* params, const pa_
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, ws);
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
-  return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots, st));
+  return cuda_status(
+      run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(ws, batch, r), st));
 }

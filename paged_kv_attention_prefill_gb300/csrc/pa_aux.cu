@@ -3,6 +3,28 @@
 
 namespace pa {
 
+// In-place descending bitonic sort of npow (a power of two) keys in shared
+// memory by one 1024-thread CTA.
+__device__ void bitonic_sort_desc(unsigned long long* keys, int npow) {
+  const int tid = threadIdx.x;
+  for (int k = 2; k <= npow; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < npow; i += 1024) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            keys[i] = y;
+            keys[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Plan: classify rows and lay out the work of one call (one CTA).
 //
@@ -98,22 +120,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
   }
   __syncthreads();
   if (s_bad) return;
-  for (int k = 2; k <= npow; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < npow; i += 1024) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long x = keys[i], y = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? (x < y) : (x > y)) {
-            keys[i] = y;
-            keys[ixj] = x;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
+  bitonic_sort_desc(keys, npow);
   for (int i = tid; i < n; i += 1024) {
     const unsigned long long key = keys[i];
     tiles[i] = make_int2((int)((key >> 12) & 0xFFFFFu), (int)(key & 0xFFFu));
@@ -127,6 +134,47 @@ cudaError_t launch_plan(const AttnArgs& a, int mode_mixed, int max_decode_q, int
                                   const_cast<int32_t*>(a.dec_base),
                                   const_cast<int32_t*>(a.slot_tok), const_cast<int2*>(a.tiles),
                                   max_tiles, a.max_slots);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Decode work order.  The persistent decode kernel hands out its items
+// (row, KV head, split, row block) in row order; listing the rows whose
+// splits hold the most keys first (longest processing time first) keeps the
+// items taken last short, so fewer warps idle at the end of the call.  Items
+// are independent, so the order changes no result.  Rows off the decode
+// path (mixed calls) go last; ties keep row order.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) row_order_kernel(const AttnArgs a, int32_t* order) {
+  __shared__ unsigned long long keys[MAX_ORDER_ROWS];
+  const Problem& p = a.p;
+  const int n = p.num_rows;  // 2 .. MAX_ORDER_ROWS, checked by the host
+  int npow = 2;
+  while (npow < n) npow <<= 1;
+  for (int i = threadIdx.x; i < npow; i += 1024) {
+    unsigned long long key = 0ull;  // padding sorts below every row
+    if (i < n) {
+      const int qs = p.cu_q[i], qb = p.cu_q[i + 1] - qs;
+      const bool dec = qb >= 1 && qs >= 0 && qs + qb <= p.total_q &&
+                       (a.dec_base == nullptr || a.dec_base[i] >= 0);
+      unsigned work = 0;
+      if (dec) {
+        const int L = max(p.seq_lens[i], 0);
+        const int n_tiles = (L + DEC_KT - 1) / DEC_KT;
+        work = (unsigned)((n_tiles + NSPLIT - 1) / NSPLIT) + 1u;
+      }
+      key = ((unsigned long long)work << 32) | (unsigned)(n - i);
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  bitonic_sort_desc(keys, npow);
+  for (int i = threadIdx.x; i < n; i += 1024) order[i] = n - (int)(keys[i] & 0xFFFFFFFFull);
+}
+
+cudaError_t launch_row_order(const AttnArgs& a, int32_t* order, cudaStream_t st) {
+  if (a.p.num_rows < 2 || a.p.num_rows > MAX_ORDER_ROWS) return cudaErrorInvalidValue;
+  row_order_kernel<<<1, 1024, 0, st>>>(a, order);
   return cudaGetLastError();
 }
 

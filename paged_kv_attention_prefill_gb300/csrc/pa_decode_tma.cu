@@ -141,6 +141,7 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
   rest /= NSPLIT;
   f.kh = rest % p.hkv;
   f.b = rest / p.hkv;
+  if (a.row_order) f.b = __ldg(a.row_order + f.b);
   f.qs = __ldg(p.cu_q + f.b);
   f.qb = __ldg(p.cu_q + f.b + 1) - f.qs;
   if (f.qb <= 0 || f.qs < 0 || f.qs + f.qb > p.total_q) return false;
@@ -297,7 +298,6 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
   // operand slots (2tig, 2tig+1 | 2tig+8, 2tig+9) hold head-dim columns
   // 4tig .. 4tig+3, and Q's fragments are loaded with the same order.
   constexpr int G = C::G;
-  constexpr int NACC = G == 1 && D <= 128 ? 2 : 1;  // accumulator sets per slot for S^T
   uint32_t phase = 0;                   // bit s: parity of ring slot s
   bool aborted = false;
   int it_id = -1;
@@ -388,6 +388,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
     // unrolled MMA sequences carry no branches.
     auto math = [&](auto nt_const) {
       constexpr int NT = decltype(nt_const)::value;
+      // accumulator sets per slot for S^T: two shorten the dependent MMA
+      // chain where registers allow (one n-tile, or d <= 128)
+      constexpr int NACC = G == 1 && (NT == 1 || D <= 128) ? 2 : 1;
       // S^T = K Q^T.  ldmatrix x4 at segments (sb, sb+1): lanes 0-15 address
       // key rows 0-15 of segment sb, lanes 16-31 of segment sb+1.
       float sa[G][NACC][NT][4];

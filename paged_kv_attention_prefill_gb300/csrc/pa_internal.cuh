@@ -42,6 +42,7 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct WsLayout {
   size_t dec_base;   // int32 [num_rows]   partial-slot base of each decode row, -1 otherwise
+  size_t row_order;  // int32 [num_rows]   decode rows, longest split first
   size_t slot_tok;   // int32 [max_slots]  global token of each decode slot
   size_t tiles;      // int2  [max_tiles]  (row, m-block) prefill work items
   size_t part_acc;   // float [max_slots, Hq, NSPLIT, d]
@@ -86,6 +87,7 @@ struct AttnArgs {
   float2* part_ml;
   const int32_t* dec_base;   // mixed: slot base per row (-1: not a decode row); null: slot = token
   const int32_t* slot_tok;   // mixed: global token per slot; null: slot = token
+  const int32_t* row_order;  // decode work order of the rows; null: row order
   const int2* tiles;         // prefill work list
   const uint32_t* n_tiles;   // its length (device)
   int max_decode_q;
@@ -101,6 +103,10 @@ cudaError_t launch_decode_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int 
 cudaError_t launch_prefill_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int max_tiles,
                                cudaStream_t st);
 cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream_t st);
+// Rows with more work per decode split first (rows off the decode path
+// last); written to `order` for 2 <= num_rows <= MAX_ORDER_ROWS.
+constexpr int MAX_ORDER_ROWS = 4096;
+cudaError_t launch_row_order(const AttnArgs& a, int32_t* order, cudaStream_t st);
 cudaError_t launch_f32(const AttnArgs& a, int decode_mode, int grid_x, int n_mblk,
                        cudaStream_t st);
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int d);

@@ -100,6 +100,28 @@ def test_decode_small(dtype, kv, d):
     assert max_err(out, ref_of(cpu)) <= tol
 
 
+@pytest.mark.parametrize("entry", ["decode", "mixed"])
+@pytest.mark.parametrize("kv", [None, "e5m2"])
+def test_decode_many_rows_work_order(entry, kv):
+    # enough rows that the decode work is handed out longest-split-first:
+    # every row, whatever its place in that order, matches the oracle, and
+    # equals the same row computed alone
+    g = torch.Generator().manual_seed(77)
+    n = 40
+    kl = torch.randint(0, 3000, (n,), generator=g).tolist()
+    kl[:4] = [0, 1, 2999, 64]
+    ql = [1 + (i % 3 == 0) for i in range(n)]
+    if entry == "mixed":
+        ql[5], kl[5] = 40, 700      # a prefill row among the decode rows
+    cpu, gpu = small(ql, kl, hq=8, hkv=2, d=128, P=16, dtype="f16", kv_dtype=kv, seed=31)
+    out = run(entry, gpu)
+    assert max_err(out, ref_of(cpu)) <= tol_of(cpu)
+    cu = cpu.cu_seqlens_q.tolist()
+    for r in (2, 17, 39):
+        alone = run(entry, workloads.sub_batch(cpu, [r]).to("cuda"))
+        assert_bitwise(out[cu[r]:cu[r + 1]], alone)
+
+
 @pytest.mark.parametrize("dtype,kv", [("bf16", None), ("f16", "e5m2"), ("f32", None)])
 def test_mixed_small_and_routing_bitwise(dtype, kv):
     ql = [300, 1, 4, 0, 17, 16, 2]
