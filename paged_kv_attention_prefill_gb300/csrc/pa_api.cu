@@ -47,6 +47,7 @@ struct Resolved {
   int host_tiles;     // prefill work items (host mirrors), for the tile height in use
   int host_slots;     // decode slots (host mirrors)
   bool tc;            // prefill on the tcgen05 kernel
+  bool tc2;           // prefill on the two-tile tcgen05 kernel
   int pf_bm;          // query rows per prefill work item
 };
 
@@ -121,8 +122,10 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g);
   if (ws_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
-  r->tc = prefill_tc_supported(r->qd, r->kvd, r->d, (int64_t)bat->num_pages * r->P);
-  r->pf_bm = r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
+  const int64_t cache_tokens = (int64_t)bat->num_pages * r->P;
+  r->tc2 = prefill_tc2_supported(r->qd, r->kvd, r->d, cache_tokens);
+  r->tc = !r->tc2 && prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens);
+  r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
   r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
   r->host_max_q_dec = 0;
   r->host_tiles = 0;
@@ -226,6 +229,7 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
 
 cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, cudaStream_t st) {
   if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
+  if (r.tc2) return launch_prefill_tc2(a, r.qd, grid_tiles, st);
   if (r.tc) return launch_prefill_tc(a, r.qd, grid_tiles, st);
   return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
 }

@@ -1,0 +1,538 @@
+// Varlen causal paged prefill on the tcgen05 tensor cores, two query tiles
+// per CTA (head dims 64 and 128).
+//
+// The same attention as every other path of the library (packed varlen
+// batch, one block table per row, bottom-right causal alignment, GQA, online
+// softmax over key tiles: vllm-rlt PR #128, "Purpose", prefill bullets).
+// The layout keeps the tensor core busy while the softmax of a tile runs:
+//
+//  * A CTA owns 256 GQA-packed query rows of one (row, KV head) as two
+//    128-row query tiles A and B (the heads that share the KV head stacked
+//    along M: 1Cat-vLLM PR #1279, commit 1).  Every K/V tile brought in by
+//    TMA serves both query tiles.
+//  * Warp 0 streams K tiles and warp 2 V tiles, one 16-token page slot per
+//    TMA box (1Cat-vLLM PR #616, original description: any page size that is
+//    a multiple of 16), into two shared-memory rings.  The slot that holds a
+//    row's last key is copied by hand with the keys past the end zero-filled.
+//  * Warp 1, one thread, issues tcgen05.mma for both query tiles in turn:
+//    S_t = Q_t K^T into tile t's S columns of TMEM, O_t += P_t V with P_t
+//    read from TMEM.  While one softmax warpgroup works on its S, the tensor
+//    core computes the other tile's products.
+//  * Warpgroup 1 runs the softmax of tile A, warpgroup 2 that of tile B; each
+//    thread owns one query row (one TMEM lane) over all 128 key columns, so
+//    the row maximum needs no exchange between threads.  P (16-bit) is
+//    written over S in TMEM.  O is rescaled only when a row's maximum grows
+//    by more than 2^8; the final O / l is the same.
+//  * setmaxnreg moves registers from the producer / MMA warpgroup to the two
+//    softmax warpgroups.
+//
+// Every wait is bounded (about two seconds); on a timeout the CTA raises the
+// workspace flag, drains the copies and MMAs it started, frees TMEM and
+// exits.
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+#include "pa_sm100.cuh"
+
+namespace pa {
+bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                   int64_t tokens);
+
+namespace {
+
+using namespace sm100;
+
+// Registers per thread at launch (384 threads, one CTA per SM) and after the
+// split: 128 * REG_LOW + 256 * REG_HIGH == 384 * REG_LAUNCH.
+constexpr int REG_LAUNCH = 168, REG_LOW = 56, REG_HIGH = 224;
+static_assert(128 * REG_LOW + 256 * REG_HIGH == 384 * REG_LAUNCH, "register split");
+
+template <int D>
+struct Tc2Cfg {
+  static constexpr int BM = 128;                    // rows per query tile = TMEM lanes
+  static constexpr int BN = 128;                    // keys per tile
+  static constexpr int KS = D == 64 ? 4 : 2;        // K ring stages
+  static constexpr int VS = D == 64 ? 4 : 3;        // V ring stages
+  static constexpr int NCH = D / 64;                // 128-byte column chunks of d
+  static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
+  static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
+  static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one key tile
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+  static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
+  // TMEM: tile t owns columns [t * TILE_COLS, +BN) for S (P over it) and
+  // [t * TILE_COLS + BN, +D) for O.
+  static constexpr uint32_t TILE_COLS = BN + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // barrier indices
+  static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
+                       B_SF = 2 * KS + 2 * VS,  // [2] S_t written
+      B_PF = B_SF + 2,                          // [2] P_t written (128 arrivals)
+      B_OF = B_PF + 2,                          // [2] O_t += P_t V done
+      B_Q = B_OF + 2,                           // [2] Q_t staged (128 arrivals)
+      B_DRAIN = B_Q + 2, NBAR = B_DRAIN + 1;
+  static_assert(2 * TILE_COLS <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NBAR * 8 <= 240, "barrier area");
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(384, 1)
+    prefill_tc2_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV) {
+  using C = Tc2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+  const Problem& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item (uniform over the CTA) -----------------------------------
+  // 1-D grid, KV head slowest; the work list is longest-first
+  const int n_items = (int)(gridDim.x / p.hkv);
+  const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
+  if (item >= (int)*a.n_tiles) return;
+  const int2 wi = a.tiles[item];
+  const int b = wi.x, mb = wi.y;
+  const int qs = __ldg(p.cu_q + b);
+  const int qb = __ldg(p.cu_q + b + 1) - qs;
+  const int L = __ldg(p.seq_lens + b);
+  if (qb <= 0) return;
+  if (qs < 0 || qs + qb > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return;
+  }
+  const int g = p.g, M = qb * g, R0 = mb * 2 * C::BM;
+  if (R0 >= M) return;
+  // key tiles of each query tile (0 for an empty tile B)
+  auto tiles_of = [&](int r0) {
+    if (r0 >= M) return 0;
+    const int r_last = min(r0 + C::BM, M) - 1;
+    const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile sees
+    return k_end > 0 ? (k_end + C::BN - 1) / C::BN : 0;
+  };
+  const int nA = tiles_of(R0), nB = tiles_of(R0 + C::BM);
+  const int n_kv = max(nA, nB);
+
+  // ---- barriers and TMEM ----------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(bar(C::B_KF + s), 1);
+      mbar_init(bar(C::B_KE + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      mbar_init(bar(C::B_VF + s), 1);
+      mbar_init(bar(C::B_VE + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_SF + t), 1);
+      mbar_init(bar(C::B_PF + t), 128);
+      mbar_init(bar(C::B_OF + t), 1);
+      mbar_init(bar(C::B_Q + t), 128);
+    }
+    mbar_init(bar(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    setmaxnreg_dec<REG_LOW>();
+    if (warp == 0 || warp == 2) {
+      // ============ producers: warp 0 streams K tiles, warp 2 V tiles ========
+      const bool isK = warp == 0;
+      const int NS = isK ? C::KS : C::VS;
+      const int B_FULL = isK ? C::B_KF : C::B_VF, B_EMPTY = isK ? C::B_KE : C::B_VE;
+      const uint32_t ring = isK ? sK : sV;
+      const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+      const T* cache = static_cast<const T*>(isK ? a.kc : a.vc);
+      if (lane == 0) tma_prefetch_desc(tmap);
+      const int P = p.page_size;
+      const int64_t bt_row = (int64_t)b * p.max_pages;
+      int j = 0;
+      bool ok = true;
+      for (; j < n_kv; ++j) {
+        const int st = j % NS;
+        if (j >= NS) ok = mbar_wait(bar(B_EMPTY + st), ((j / NS) - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const int kbase = j * C::BN;
+        const uint32_t dst = ring + st * C::KV_BYTES;
+        // slot `lane`: 1 = whole slot by TMA, 2 = partial (copied by hand), 3 = zero-fill
+        int kind = 0, tok0 = 0;
+        if (lane < C::SLOTS) {
+          const int s0 = kbase + 16 * lane;
+          if (s0 >= L) {
+            kind = 3;
+          } else {
+            const int col = s0 / P;
+            const int page = col < p.max_pages ? __ldg(p.bt + bt_row + col) : -1;
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+              kind = 3;
+            } else {
+              tok0 = page * P + (s0 % P);
+              kind = (s0 + 16 <= L) ? 1 : 2;
+            }
+          }
+        }
+        uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
+        while (manual) {
+          const int s = __ffs(manual) - 1;
+          manual &= manual - 1;
+          const int ks = __shfl_sync(0xffffffffu, kind, s);
+          const int t0 = __shfl_sync(0xffffffffu, tok0, s);
+          const int nvalid = ks == 2 ? L - (kbase + 16 * s) : 0;
+          for (int it = lane; it < 16 * C::NCH * 8; it += 32) {
+            const int piece = it & 7, rest = it >> 3;
+            const int c = rest % C::NCH, rr = rest / C::NCH;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (rr < nvalid) {
+              const T* src = cache + ((int64_t)(t0 + rr) * p.hkv + kh) * D + c * 64 + piece * 8;
+              v = __ldg(reinterpret_cast<const uint4*>(src));
+            }
+            const int row = 16 * s + rr;
+            st_shared_v4(dst + c * (C::BN * 128) + row * 128 + ((piece ^ (row & 7)) << 4), v);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + st), (uint32_t)n_tma * 16u * D * 2u);
+        __syncwarp();
+        if (kind == 1) {
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(dst + c * (C::BN * 128) + lane * 16 * 128, tmap, c * 64, kh, tok0,
+                        bar(B_FULL + st));
+        }
+      }
+      if (!ok) {
+        // copies this warp started may still be landing: wait for them
+        for (int jj = max(0, j - NS); jj < j; ++jj)
+          mbar_drain(bar(B_FULL + jj % NS), (jj / NS) & 1, p.err);
+      }
+    } else if (warp == 1) {
+      // ===================== MMA issuer (one thread) ===========================
+      // Event-driven: each pass issues whatever is ready, P V of a tile first
+      // (it completes the tile's step), then the tile's next S.  S_t(j+1)
+      // overwrites the columns that hold P_t(j), so it waits for
+      // O_t += P_t(j) V to complete.  A K (V) stage is released once both
+      // tiles have issued their products with it.
+      if (lane == 0) {
+        constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+        constexpr uint32_t idS = idesc_f16(fmt, 128, C::BN, false);
+        constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
+        bool ok = true;
+        if (nA > 0) ok = mbar_wait(bar(C::B_Q + 0), 0, abort_flag, p.err);
+        if (ok && nB > 0) ok = mbar_wait(bar(C::B_Q + 1), 0, abort_flag, p.err);
+        if (ok) tc_fence_after();
+        int sj[2] = {0, 0}, pj[2] = {0, 0};  // next S / P V index of each tile
+        const int ntl[2] = {nA, nB};
+        int k_rel = 0, v_rel = 0;            // next K / V tile to release
+        long long idle_since = clock64();
+        while (ok) {
+          bool progress = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t tb = tmem + t * C::TILE_COLS;
+            if (pj[t] < sj[t]) {
+              const int j = pj[t], sv = j % C::VS;
+              if (mbar_test_wait(bar(C::B_PF + t), j & 1) &&
+                  mbar_test_wait(bar(C::B_VF + sv), (j / C::VS) & 1)) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < C::BN / 16; ++k) {
+                  // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
+                  const uint64_t bd =
+                      sdesc_sw128(sV + sv * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
+                  tc_mma_f16_ts(tb + C::BN, tb + 8 * k, bd, idO, (j > 0 || k > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(C::B_OF + t));
+                ++pj[t];
+                progress = true;
+              }
+            }
+            if (sj[t] < ntl[t] && sj[t] == pj[t]) {
+              const int j = sj[t], st = j % C::KS;
+              if (mbar_test_wait(bar(C::B_KF + st), (j / C::KS) & 1) &&
+                  (j == 0 || mbar_test_wait(bar(C::B_OF + t), (j - 1) & 1))) {
+                tc_fence_after();
+                const uint32_t q_t = sQ + t * C::Q_BYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                  const uint64_t ad =
+                      sdesc_sw128(q_t + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+                  const uint64_t bd = sdesc_sw128(
+                      sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+                  tc_mma_f16(tb, ad, bd, idS, k > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(C::B_SF + t));
+                ++sj[t];
+                progress = true;
+              }
+            }
+          }
+          while (k_rel < n_kv && (k_rel < sj[0] || k_rel >= nA) && (k_rel < sj[1] || k_rel >= nB)) {
+            tc_commit(bar(C::B_KE + k_rel % C::KS));
+            ++k_rel;
+          }
+          while (v_rel < n_kv && (v_rel < pj[0] || v_rel >= nA) && (v_rel < pj[1] || v_rel >= nB)) {
+            tc_commit(bar(C::B_VE + v_rel % C::VS));
+            ++v_rel;
+          }
+          if (pj[0] == nA && pj[1] == nB && k_rel == n_kv && v_rel == n_kv) break;
+          if (progress) {
+            idle_since = clock64();
+          } else if (*abort_flag) {
+            ok = false;
+          } else if (clock64() - idle_since > WAIT_LIMIT_CYCLES) {
+            *abort_flag = 1;
+            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            ok = false;
+          }
+        }
+        // nothing this thread issued may still run once TMEM is freed
+        tc_commit(bar(C::B_DRAIN));
+        mbar_drain(bar(C::B_DRAIN), 0, p.err);
+      }
+      __syncwarp();
+    }
+  } else {
+    setmaxnreg_inc<REG_HIGH>();
+    // ============ softmax and epilogue of query tile t ========================
+    // Thread = one query row = one TMEM lane of the tile.  The loop never
+    // leaves early: after a timed-out wait it runs on (flag raised, waits
+    // return at once), so the CTA always reaches its final barrier.
+    const int t = (warp >> 2) - 1;
+    const int q4 = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q4 * 32 + lane;     // row of the tile == TMEM lane
+    const int R = R0 + t * C::BM + r;
+    const bool valid = R < M;
+    const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
+    const int last = valid ? L - qb + i : -1;  // last visible key of this row
+    const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
+    const int n = t ? nB : nA;
+    const uint32_t q_t = sQ + t * C::Q_BYTES;
+    if (n > 0) {
+      const T* qrow = static_cast<const T*>(a.q) + qoff;
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) {
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc) {
+          const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + pc * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(q_t + c * (C::BM * 128) + r * 128 + ((pc ^ (r & 7)) << 4), v);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_Q + t));
+    }
+    const uint32_t trow = tmem + t * C::TILE_COLS + ((uint32_t)(q4 * 32) << 16);
+    const float sl2 = p.sl2;
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      mbar_wait(bar(C::B_SF + t), j & 1, abort_flag, p.err);
+      tc_fence_after();
+      // S_t(j) was issued after O_t += P_t(j-1) V completed, and its commit
+      // covers every earlier MMA: O_t is stable here.
+      float x[C::BN];
+      {
+        uint32_t u[C::BN];
+        tmem_ld_x128(trow, u);
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k) x[k] = __uint_as_float(u[k]);
+      }
+      const int kb = j * C::BN;
+      if (kb + C::BN - 1 > last) {
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k)
+          if (kb + k > last) x[k] = -INFINITY;
+      }
+      float mt;  // max raw logit of the row in this tile (masked keys -> -inf)
+      {
+        float pm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+#pragma unroll
+        for (int k = 8; k < C::BN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      }
+      const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
+      float factor = 1.f;
+      bool need = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + 8.f) {
+        need = true;
+        factor = ex2(m_used - m_new);
+        m_used = m_new;
+      }
+      const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+#pragma unroll
+      for (int k = 0; k < C::BN; ++k) {
+        x[k] = ex2(fmaf(x[k], sl2, nmu));
+        ps[k & 7] += x[k];
+      }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::BN + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tmem_st_x32(trow + C::BN + c * 32, o);
+        }
+      }
+      l = l * factor + rs;
+      {
+        // P (16-bit pairs) over the first BN / 2 columns of S
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) pk[k] = pack2<T>(x[64 * h + 2 * k], x[64 * h + 2 * k + 1]);
+          tmem_st_x32_nowait(trow + 32 * h, pk);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PF + t));
+    }
+    // ---- epilogue: out = O / l * v_scale ----
+    T* orow = static_cast<T*>(a.out) + qoff;
+    if (n > 0) {
+      mbar_wait(bar(C::B_OF + t), (n - 1) & 1, abort_flag, p.err);
+      tc_fence_after();
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_x32(trow + C::BN + c * 32, o);
+        if (valid) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 v;
+            v.x = pack2<T>(__uint_as_float(o[8 * w + 0]) * inv, __uint_as_float(o[8 * w + 1]) * inv);
+            v.y = pack2<T>(__uint_as_float(o[8 * w + 2]) * inv, __uint_as_float(o[8 * w + 3]) * inv);
+            v.z = pack2<T>(__uint_as_float(o[8 * w + 4]) * inv, __uint_as_float(o[8 * w + 5]) * inv);
+            v.w = pack2<T>(__uint_as_float(o[8 * w + 6]) * inv, __uint_as_float(o[8 * w + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * w) = v;
+          }
+        }
+      }
+    } else if (valid) {
+      // no key visible to any row of the tile
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
+                       cudaStream_t st) {
+  using C = Tc2Cfg<D>;
+  auto k = prefill_tc2_kernel<T, D>;
+  static DeviceFlags attr;
+  cudaError_t e = attr.once([&] {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  });
+  if (e != cudaSuccess) return e;
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, C::SMEM, st>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+bool regs_ok() {
+  // the register split is only safe when the kernel launches with exactly
+  // REG_LAUNCH registers per thread
+  static int ok = -1;
+  if (ok < 0) {
+    cudaFuncAttributes fa{};
+    ok = cudaFuncGetAttributes(&fa, prefill_tc2_kernel<T, D>) == cudaSuccess &&
+         fa.numRegs == REG_LAUNCH;
+  }
+  return ok == 1;
+}
+
+}  // namespace
+
+bool prefill_tc2_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
+  if (!((q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype && (d == 64 || d == 128) &&
+        cache_tokens < (int64_t(1) << 31)))
+    return false;
+  const bool bf = q_dtype == PA_BF16;
+  if (d == 64) return bf ? regs_ok<__nv_bfloat16, 64>() : regs_ok<__half, 64>();
+  return bf ? regs_ok<__nv_bfloat16, 128>() : regs_ok<__half, 128>();
+}
+
+cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st) {
+  if (grid_x == 0) return cudaSuccess;
+  const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
+  CUtensorMap tk, tv;
+  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+    return cudaErrorInvalidValue;
+  const bool bf = q_dtype == PA_BF16;
+  switch (a.p.d) {
+    case 64: return bf ? launch_tc2<__nv_bfloat16, 64>(a, tk, tv, grid_x, st)
+                       : launch_tc2<__half, 64>(a, tk, tv, grid_x, st);
+    case 128: return bf ? launch_tc2<__nv_bfloat16, 128>(a, tk, tv, grid_x, st)
+                        : launch_tc2<__half, 128>(a, tk, tv, grid_x, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa
