@@ -44,9 +44,10 @@ namespace {
 using namespace sm100;
 
 // Registers per thread at launch (384 threads, one CTA per SM) and after the
-// split: 128 * REG_LOW + 256 * REG_HIGH == 384 * REG_LAUNCH.
-constexpr int REG_LAUNCH = 168, REG_LOW = 56, REG_HIGH = 224;
-static_assert(128 * REG_LOW + 256 * REG_HIGH == 384 * REG_LAUNCH, "register split");
+// split, which must fit in what the CTA was launched with:
+// 128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH.
+constexpr int REG_LAUNCH = 168, REG_LOW = 64, REG_HIGH = 216;
+static_assert(128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH, "register split");
 
 template <int D>
 struct Tc2Cfg {
@@ -254,83 +255,76 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1) {
       // ===================== MMA issuer (one thread) ===========================
-      // Event-driven: each pass issues whatever is ready, P V of a tile first
-      // (it completes the tile's step), then the tile's next S.  S_t(j+1)
-      // overwrites the columns that hold P_t(j), so it waits for
-      // O_t += P_t(j) V to complete.  A K (V) stage is released once both
-      // tiles have issued their products with it.
+      // In-order, with blocking waits: per key tile j and query tile t,
+      //   O_t += P_t(j) V   once P_t(j) is written, then
+      //   S_t(j+1)          once that product is done (S_t(j+1) overwrites
+      //                     the columns P_t(j) is read from),
+      // tile A first.  The commit of S_t(j+1) covers the P V product before
+      // it, so when the softmax sees S_t(j+1), O_t is stable.  A K (V) stage
+      // is released once both tiles have issued their products with it.
       if (lane == 0) {
         constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
         constexpr uint32_t idS = idesc_f16(fmt, 128, C::BN, false);
         constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
-        bool ok = true;
-        if (nA > 0) ok = mbar_wait(bar(C::B_Q + 0), 0, abort_flag, p.err);
-        if (ok && nB > 0) ok = mbar_wait(bar(C::B_Q + 1), 0, abort_flag, p.err);
-        if (ok) tc_fence_after();
-        int sj[2] = {0, 0}, pj[2] = {0, 0};  // next S / P V index of each tile
         const int ntl[2] = {nA, nB};
-        int k_rel = 0, v_rel = 0;            // next K / V tile to release
-        long long idle_since = clock64();
-        while (ok) {
-          bool progress = false;
+        auto issue_S = [&](int t, int j) {
+          const int st = j % C::KS;
+          if (!mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err)) return false;
+          tc_fence_after();
+          const uint32_t q_t = sQ + t * C::Q_BYTES;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t ad =
+                sdesc_sw128(q_t + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(
+                sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+            tc_mma_f16(tmem + t * C::TILE_COLS, ad, bd, idS, k > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_SF + t));
+          return true;
+        };
+        auto issue_PV = [&](int t, int j) {
+          const int sv = j % C::VS;
+          if (!mbar_wait(bar(C::B_PF + t), j & 1, abort_flag, p.err) ||
+              !mbar_wait(bar(C::B_VF + sv), (j / C::VS) & 1, abort_flag, p.err))
+            return false;
+          tc_fence_after();
+          const uint32_t tb = tmem + t * C::TILE_COLS;
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
+            const uint64_t bd = sdesc_sw128(sV + sv * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
+            tc_mma_f16_ts(tb + C::BN, tb + 8 * k, bd, idO, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_OF + t));
+          return true;
+        };
+        bool ok = true;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && ntl[t] > 0) ok = mbar_wait(bar(C::B_Q + t), 0, abort_flag, p.err);
+        if (ok) tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ok && ntl[t] > 0) ok = issue_S(t, 0);
+        if (ok && n_kv > 0) tc_commit(bar(C::B_KE + 0));
+        for (int j = 0; ok && j < n_kv; ++j) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            const uint32_t tb = tmem + t * C::TILE_COLS;
-            if (pj[t] < sj[t]) {
-              const int j = pj[t], sv = j % C::VS;
-              if (mbar_test_wait(bar(C::B_PF + t), j & 1) &&
-                  mbar_test_wait(bar(C::B_VF + sv), (j / C::VS) & 1)) {
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < C::BN / 16; ++k) {
-                  // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
-                  const uint64_t bd =
-                      sdesc_sw128(sV + sv * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-                  tc_mma_f16_ts(tb + C::BN, tb + 8 * k, bd, idO, (j > 0 || k > 0) ? 1u : 0u);
+            if (ok && j < ntl[t]) {
+              ok = issue_PV(t, j);
+              if (ok && j + 1 < ntl[t]) {
+                ok = mbar_wait(bar(C::B_OF + t), j & 1, abort_flag, p.err);
+                if (ok) {
+                  tc_fence_after();
+                  ok = issue_S(t, j + 1);
                 }
-                tc_commit(bar(C::B_OF + t));
-                ++pj[t];
-                progress = true;
-              }
-            }
-            if (sj[t] < ntl[t] && sj[t] == pj[t]) {
-              const int j = sj[t], st = j % C::KS;
-              if (mbar_test_wait(bar(C::B_KF + st), (j / C::KS) & 1) &&
-                  (j == 0 || mbar_test_wait(bar(C::B_OF + t), (j - 1) & 1))) {
-                tc_fence_after();
-                const uint32_t q_t = sQ + t * C::Q_BYTES;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                  const uint64_t ad =
-                      sdesc_sw128(q_t + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
-                  const uint64_t bd = sdesc_sw128(
-                      sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
-                  tc_mma_f16(tb, ad, bd, idS, k > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(C::B_SF + t));
-                ++sj[t];
-                progress = true;
               }
             }
           }
-          while (k_rel < n_kv && (k_rel < sj[0] || k_rel >= nA) && (k_rel < sj[1] || k_rel >= nB)) {
-            tc_commit(bar(C::B_KE + k_rel % C::KS));
-            ++k_rel;
-          }
-          while (v_rel < n_kv && (v_rel < pj[0] || v_rel >= nA) && (v_rel < pj[1] || v_rel >= nB)) {
-            tc_commit(bar(C::B_VE + v_rel % C::VS));
-            ++v_rel;
-          }
-          if (pj[0] == nA && pj[1] == nB && k_rel == n_kv && v_rel == n_kv) break;
-          if (progress) {
-            idle_since = clock64();
-          } else if (*abort_flag) {
-            ok = false;
-          } else if (clock64() - idle_since > WAIT_LIMIT_CYCLES) {
-            *abort_flag = 1;
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
-            ok = false;
-          }
+          if (!ok) break;
+          tc_commit(bar(C::B_VE + j % C::VS));
+          if (j + 1 < n_kv) tc_commit(bar(C::B_KE + (j + 1) % C::KS));
         }
         // nothing this thread issued may still run once TMEM is freed
         tc_commit(bar(C::B_DRAIN));
