@@ -120,9 +120,9 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item (uniform over the CTA) -----------------------------------
-  // 1-D grid, KV head slowest; the work list is longest-first
-  const int n_items = (int)(gridDim.x / p.hkv);
-  const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
+  // 1-D grid, KV head fastest: the work list is longest-first, so the CTAs
+  // dispatched last are the shortest of all heads
+  const int item = blockIdx.x / p.hkv, kh = blockIdx.x % p.hkv;
   if (item >= (int)*a.n_tiles) return;
   const int2 wi = a.tiles[item];
   const int b = wi.x, mb = wi.y;
