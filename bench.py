@@ -46,14 +46,14 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # DRAM bytes (read + write) per launch of the prefill kernel on this workload,
-# from the ncu capture summarised in profiles/prefill_tc_workload2.md.  Reported
-# only while the kernel's sources are the ones that were profiled.
+# from the ncu capture summarised in profiles/prefill_tc2_workload2.md.
+# Reported only while the kernel's sources are the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc.cu": "83ee3f6ef78ac3df5867f9cd9623edd8e6a87deeec98749a1e0460c8311f0fed",
-        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "a0c3f742d599cb59e88fbba788f02b84fb6cdc49843e0cc8eda785ab5bf4decd",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "be9d5d1d4e7436341782b95b8ce43f20a125248f09c0dfc67f60f02d82ff71b3",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "f3adf47265b0acda2025bac2ca22fb1aaeddec86e8d55801cc41b513356c6166",
     },
-    "bytes_per_launch": 465146624,
+    "bytes_per_launch": 959060480 + 54701312,
 }
 
 
@@ -153,10 +153,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def launches_per_call(q_lens, max_dq=16):
-    dec = any(1 <= q <= max_dq for q in q_lens)
-    pre = any(q > max_dq for q in q_lens)
-    return 1 + (2 if dec else 0) + (1 if pre else 0)
+def launches_per_call(q_lens, max_dq=16, mixed=True):
+    """Kernels one call launches: the plan (mixed and prefill calls), then for
+    decode rows the work-order sort (16 or more rows in the call), the decode
+    kernel and the merge, then the prefill kernel."""
+    n_rows = len(q_lens)
+    dec = any(1 <= q <= max_dq for q in q_lens) if mixed else n_rows > 0
+    pre = mixed and any(q > max_dq for q in q_lens)
+    n = 1 if mixed else 0
+    if dec:
+        n += 2 + (1 if n_rows >= 16 else 0)
+    return n + (1 if pre else 0)
 
 
 def call_args(b):
@@ -203,7 +210,7 @@ def part_decode(n, steps, warmup, stream, pk):
     gbs = byt / (ms * 1e-3) / 1e9
     res = {"workload": workloads.WORKLOADS[n], "ms": round(ms, 4), "kv_bytes": byt,
            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
-           "launches_per_call": 2}
+           "launches_per_call": launches_per_call(b.q_lens, mixed=False)}
     del b, ws, out
     torch.cuda.empty_cache()
     return res
@@ -359,7 +366,7 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                          "peak": pk["bf16"], "unit": "TFLOP/s",
                          "frac": round(achieved / pk["bf16"], 4), "traffic": profiled_traffic(),
-                         "kernel": "prefill (whole call timed: routing kernel included)",
+                         "kernel": "prefill_tc2_kernel (whole call timed: routing kernel included)",
                          "peak_source": f"{pk['source']} bf16 burst"},
             "cpu_baseline": {"value": round(cpu_val, 6), "unit": "TFLOP/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
