@@ -193,6 +193,20 @@ def time_calls(fn, steps, warmup, stream, sampler=None):
     return start.elapsed_time(end) / steps
 
 
+def graph_ms(fn, steps, warmup, stream):
+    """Times `steps` replays of a CUDA graph holding one call of fn (the call
+    runs once outside the capture first, for its one-time set-up)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    ms = time_calls(g.replay, steps, warmup, stream)
+    del g
+    return ms
+
+
 def part_decode(n, steps, warmup, stream, pk):
     import paged_kv_attention_prefill_gb300 as pa
     b = workloads.make_workload(n, device="cuda", data_device="cuda")
@@ -204,12 +218,14 @@ def part_decode(n, steps, warmup, stream, pk):
         pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
                              b.seq_lens, out=out, workspace=ws, **kw)
     ms = time_calls(fn, steps, warmup, stream)
+    ms_graph = graph_ms(fn, steps, warmup, stream)
     byt = metrics.decode_bytes(b.q_lens, b.kv_lens, num_q_heads=b.num_q_heads,
                                num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
                                q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, page_size=b.page_size)
     gbs = byt / (ms * 1e-3) / 1e9
     res = {"workload": workloads.WORKLOADS[n], "ms": round(ms, 4), "kv_bytes": byt,
            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+           "graph_replay_GB/s": round(byt / (ms_graph * 1e-3) / 1e9, 1),
            "launches_per_call": launches_per_call(b.q_lens, mixed=False)}
     del b, ws, out
     torch.cuda.empty_cache()
@@ -235,6 +251,28 @@ def part_mixed3(steps, warmup, stream, pk):
     res = {"workload": workloads.WORKLOADS[3], "ms": round(ms, 4), "prefill_flops": F,
            "decode_bytes": byt, "whole_call_TFLOP/s_of_prefill": round(F / (ms * 1e-3) / 1e12, 1),
            "launches_per_call": launches_per_call(ql)}
+    # each half as a call of its own: the chunk's row through the prefill
+    # entry, the three resident rows through the decode entry
+    for name, rows, entry in (("prefill_row_alone", [0], pa.paged_attn_prefill),
+                              ("decode_rows_alone", [1, 2, 3], pa.paged_attn_decode)):
+        sb = workloads.sub_batch(b, rows, device="cuda")
+        sws = pa.make_workspace(pa.make_params(sb.q, sb.k_cache), sb.num_rows, sb.total_q, "cuda")
+        sout = torch.empty_like(sb.q)
+        skw = call_args(sb)
+
+        def sfn():
+            entry(sb.q, sb.k_cache, sb.v_cache, sb.block_table, sb.cu_seqlens_q, sb.seq_lens,
+                  out=sout, workspace=sws, **skw)
+        sms = time_calls(sfn, steps, warmup, stream)
+        if name.startswith("prefill"):
+            tf = F / (sms * 1e-3) / 1e12
+            res[name] = {"ms": round(sms, 4), "TFLOP/s": round(tf, 1),
+                         "frac_of_bf16_peak": round(tf / pk["bf16"], 4)}
+        else:
+            gbs = byt / (sms * 1e-3) / 1e9
+            res[name] = {"ms": round(sms, 4), "GB/s": round(gbs, 1),
+                         "frac_of_hbm": round(gbs / pk["hbm"], 4)}
+        del sb, sws, sout
     del b, ws, out
     torch.cuda.empty_cache()
     return res
@@ -251,11 +289,18 @@ def part_small1(steps, warmup, stream):
         pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
                              b.seq_lens, out=out, workspace=ws, **kw)
     ms = time_calls(fn, steps, warmup, stream)
+
+    def fn_static():
+        pa.paged_attn_decode_static(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                                    b.seq_lens, out=out, **kw)
+    ms_graph = graph_ms(fn_static, steps, warmup, stream)
     return {"workload": workloads.WORKLOADS[1], "us_per_call": round(ms * 1e3, 2),
-            "note": "launch-latency bound (0.59 MB)"}
+            "graph_replay_us_per_call": round(ms_graph * 1e3, 2),
+            "note": "launch-latency bound (0.59 MB); the graph holds paged_attn_decode_static "
+                    "(no workspace argument)"}
 
 
-def cpu_baseline_sample(b, budget_s=12.0):
+def cpu_baseline_sample(b, budget_s=12.0, one_thread=True):
     """Times the oracle on sampled query tokens of the workload; returns
     (TFLOP/s, cores, description)."""
     import oracle
@@ -287,8 +332,38 @@ def cpu_baseline_sample(b, budget_s=12.0):
     t = time.perf_counter()
     oracle.paged_attention(tokens=[x[0] for x in pick], **args)
     dt = time.perf_counter() - t
-    return acc / dt / 1e12, oracle.num_threads(), \
-        f"{len(pick)} query tokens x {cpu.num_q_heads} heads of the workload ({acc:.3e} FLOP, {dt:.1f} s)"
+    cores = oracle.num_threads()  # before the one-thread run below changes it
+    extra = {"cpu_model": cpu_model(), "nproc": os.cpu_count()}
+    if one_thread:
+        # one thread, on a thirty-second of the sample
+        one = pick[: max(1, len(pick) // 32)]
+        acc1 = sum(4 * cpu.head_dim * cpu.num_q_heads * x[1] for x in one)
+        t = time.perf_counter()
+        oracle.paged_attention(tokens=[x[0] for x in one], threads=1, **args)
+        extra["one_thread_value"] = round(acc1 / (time.perf_counter() - t) / 1e12, 6)
+    return acc / dt / 1e12, cores, \
+        f"{len(pick)} query tokens x {cpu.num_q_heads} heads of the workload ({acc:.3e} FLOP, {dt:.1f} s)", \
+        extra
+
+
+def cpu_model():
+    """The host CPU's model name (x86) or architecture and part number (Arm)."""
+    import platform
+    name = part = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key = key.strip().lower()
+                if key == "model name" and not name:
+                    name = val.strip()
+                elif key == "cpu part" and not part:
+                    part = val.strip()
+    except OSError:
+        pass
+    if name:
+        return name
+    return f"{platform.machine()} (CPU part {part})" if part else platform.machine()
 
 
 def run_ours(args):
@@ -352,7 +427,7 @@ def run_ours(args):
             parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk)
             parts["mixed_chunk_plus_decode"] = part_mixed3(ps, pw, stream, pk)
             parts["decode_small_4rows"] = part_small1(max(ps, 50), 5, stream)
-        cpu_val, cores, sample = cpu_baseline_sample(b, budget_s=args.cpu_seconds)
+        cpu_val, cores, sample, cpu_extra = cpu_baseline_sample(b, budget_s=args.cpu_seconds)
         res = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -369,7 +444,7 @@ def run_ours(args):
                          "kernel": "prefill_tc2_kernel (whole call timed: routing kernel included)",
                          "peak_source": f"{pk['source']} bf16 burst"},
             "cpu_baseline": {"value": round(cpu_val, 6), "unit": "TFLOP/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, **cpu_extra},
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 3),
                     "h2d_bytes_per_step": in_bytes,
                     "d2h_bytes_per_step": out.numel() * out.element_size()},
@@ -395,7 +470,7 @@ def run_reference(args):
     budget = max(0.5, args.ref_seconds)
     vals, descr, cores = [], "", oracle.num_threads()
     for s in range(args.warmup + args.steps):
-        v, cores, descr = cpu_baseline_sample(b, budget_s=budget)
+        v, cores, descr, _ = cpu_baseline_sample(b, budget_s=budget, one_thread=False)
         if s >= args.warmup:
             vals.append(v)
     value = statistics.median(vals)

@@ -182,12 +182,13 @@ int oracle_paged_attention(const oracle_problem* p, const int32_t* cu_seqlens_q,
   const int64_t work = n_tokens * p->num_q_heads;
   const int d = p->head_dim;
 #ifdef _OPENMP
-  if (n_threads > 0) omp_set_num_threads(n_threads);
+  /* this call's team size only: later calls with n_threads <= 0 use all cores */
+  const int team = n_threads > 0 ? n_threads : omp_get_max_threads();
 #else
   (void)n_threads;
 #endif
   int err = 0;
-#pragma omp parallel
+#pragma omp parallel num_threads(team)
   {
     double* xbuf = (double*)malloc(sizeof(double) * (size_t)max_len);
     double* qv = (double*)malloc(sizeof(double) * (size_t)d);
