@@ -161,9 +161,11 @@ pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, con
 /*
  * Split-KV paged decode: every row (1 <= q_b <= max_decode_q; q_b > 1 are
  * speculative-verify rows) split into num_splits (16) contiguous parts of
- * whole 64-key tiles, chosen from L_b alone; one CTA per (row, 16-row block
- * of GQA-packed query rows, KV head, split) writes fp32 partial states; a
- * second kernel merges them in fixed split order.  Batch-invariant bitwise.
+ * whole 64-key tiles, chosen from L_b alone.  Each (row, KV head, split,
+ * 16-row block of GQA-packed query rows) is one work item; persistent warps
+ * take the items (rows with the longest splits first) and write fp32 partial
+ * states; a second kernel merges them in fixed split order.  Batch-invariant
+ * bitwise: a row's result depends on its own data and length only.
  */
 pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, const void* q,
                             const void* k_cache, const void* v_cache, void* out,
@@ -175,7 +177,12 @@ pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, cons
  * skipped.  The routing is computed on the device from cu_seqlens_q, so the
  * call needs no host mirrors and its grids depend only on num_rows and
  * total_q (capturable in a CUDA graph).  Each token's result is bitwise equal
- * to the one the corresponding single-path call gives.
+ * to the one the corresponding single-path call gives.  When the batch has
+ * both kinds of rows, the decode rows run on a second stream the library
+ * keeps per host thread and device, forked from `stream` after the routing
+ * and joined back before the call returns (event record / wait; all of the
+ * call's work is ordered before later work on `stream`, also under graph
+ * capture).
  */
 pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const void* q,
                            const void* k_cache, const void* v_cache, void* out,

@@ -197,6 +197,34 @@ int32_t* row_order_of(void* ws, const pa_batch* bat, const Resolved& r) {
 
 inline pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
+// A second stream (and two events) per host thread and device, made on first
+// use and kept for the life of the thread: a mixed call runs its decode rows
+// there, next to the prefill on the caller's stream.  Per thread, so that
+// calls from different host threads never wait on each other's work; the
+// objects are never destroyed (the driver reclaims them with the context).
+struct AuxStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+};
+AuxStream* aux_stream() {
+  thread_local AuxStream aux[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  AuxStream& x = aux[dev];
+  if (x.failed) return nullptr;
+  if (!x.st) {
+    if (cudaStreamCreateWithFlags(&x.st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) {
+      x.failed = true;
+      cudaGetLastError();
+      return nullptr;
+    }
+  }
+  return &x;
+}
+
 int decode_mblocks(const Resolved& r, int max_q) {
   return (max_q * r.g + DEC_ROWS - 1) / DEC_ROWS;
 }
@@ -302,13 +330,29 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   // decode rows: the grid covers every row; rows routed to prefill exit at once
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = r.host ? r.host_slots : (int)a.max_slots;
+  const int grid = r.host ? r.host_tiles : max_tiles;
+  // With both kinds of rows, the decode rows run on a second stream next to
+  // the prefill (they touch disjoint output rows and workspace regions): the
+  // decode kernel takes as many SMs as it has work for, the prefill CTAs the
+  // rest.  Fork after the plan, join before the call returns.
+  AuxStream* aux = (max_q > 0 && grid > 0) ? aux_stream() : nullptr;
+  cudaStream_t dst = st;
+  if (aux) {
+    if (cudaEventRecord(aux->fork, st) != cudaSuccess ||
+        cudaStreamWaitEvent(aux->st, aux->fork, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    dst = aux->st;
+  }
   if (max_q > 0) {
     e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(workspace, batch, r),
-                   st);
+                   dst);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
-  const int grid = r.host ? r.host_tiles : max_tiles;
-  return cuda_status(run_prefill(a, r, grid, st));
+  if (aux && cudaEventRecord(aux->join, aux->st) != cudaSuccess) return PA_ERR_CUDA;
+  e = run_prefill(a, r, grid, st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (aux && cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
 }
 
 pa_status paged_attn_read_errors(void* workspace, pa_stream_t stream, uint32_t* flags) {
