@@ -371,20 +371,19 @@ __global__ void __launch_bounds__(384, 1)
       // S_t(j) was issued after O_t += P_t(j-1) V completed, and its commit
       // covers every earlier MMA: O_t is stable here.
       float x[C::BN];
+      float mt;  // max raw logit of the row in this tile (masked keys -> -inf)
       {
         uint32_t u[C::BN];
-        tmem_ld_x128(trow, u);
+        mt = tmem_ld_red_max_x128(trow, u);  // the load also returns the row's max
 #pragma unroll
         for (int k = 0; k < C::BN; ++k) x[k] = __uint_as_float(u[k]);
       }
       const int kb = j * C::BN;
       if (kb + C::BN - 1 > last) {
+        // a tile on the row's diagonal: mask, and take the max of what is left
 #pragma unroll
         for (int k = 0; k < C::BN; ++k)
           if (kb + k > last) x[k] = -INFINITY;
-      }
-      float mt;  // max raw logit of the row in this tile (masked keys -> -inf)
-      {
         float pm[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) pm[u] = x[u];
