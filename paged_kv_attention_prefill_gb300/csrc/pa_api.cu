@@ -257,7 +257,7 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
 
 cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, cudaStream_t st) {
   if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
-  if (r.tc2) return launch_prefill_tc2(a, r.qd, grid_tiles, st);
+  if (r.tc2) return launch_prefill_tc2(a, r.qd, r.kvd, grid_tiles, st);
   if (r.tc) return launch_prefill_tc(a, r.qd, grid_tiles, st);
   return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
 }

@@ -114,10 +114,12 @@ bool prefill_mma_supported(int q_dtype, int kv_dtype, int d);
 constexpr int PF_BM_TC = 128;
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
 cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st);
-// tcgen05 prefill with two query tiles per CTA (16-bit, d = 64 or 128)
+// tcgen05 prefill with two query tiles per CTA (16-bit Q; same-type cache at
+// d = 64 or 128, or an fp8 E5M2 cache at d = 128)
 constexpr int PF_BM_TC2 = 256;
 bool prefill_tc2_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
-cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st);
+cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int grid_x,
+                               cudaStream_t st);
 // persistent TMA-fed split-KV decode (16-bit q; same-type or fp8 E5M2 cache)
 bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,

@@ -46,23 +46,31 @@ using namespace sm100;
 // Registers per thread at launch (384 threads, one CTA per SM) and after the
 // split, which must fit in what the CTA was launched with:
 // 128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH.
-constexpr int REG_LAUNCH = 168, REG_LOW = 64, REG_HIGH = 216;
+constexpr int REG_LAUNCH = 168, REG_LOW = 72, REG_HIGH = 216;
 static_assert(128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH, "register split");
 
-template <int D>
+template <int D, bool KV8>
 struct Tc2Cfg {
   static constexpr int BM = 128;                    // rows per query tile = TMEM lanes
   static constexpr int BN = 128;                    // keys per tile
-  static constexpr int KS = D == 64 ? 4 : 2;        // K ring stages
-  static constexpr int VS = D == 64 ? 4 : 3;        // V ring stages
+  // 16-bit K / V stages the MMAs read.  With an fp8 cache the tiles arrive as
+  // codes in their own rings (S8 stages each) and are widened into these, so
+  // fewer 16-bit stages are needed (K is read by both S products back to
+  // back; V's stage must cover the widening of the next tile).
+  static constexpr int KS = KV8 ? 1 : (D == 64 ? 4 : 2);
+  static constexpr int VS = KV8 ? 2 : (D == 64 ? 4 : 3);
+  static constexpr int S8 = KV8 ? 2 : 1;             // (one unused stage index without fp8)
   static constexpr int NCH = D / 64;                // 128-byte column chunks of d
   static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
   static constexpr uint32_t Q_BYTES = BM * D * 2;   // one query tile
-  static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one key tile
+  static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one key tile, 16-bit
+  static constexpr uint32_t KV8_BYTES = BN * D;     // K (or V) of one key tile, fp8 codes
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+  static constexpr uint32_t OFF_K8 = OFF_V + VS * KV_BYTES;
+  static constexpr uint32_t OFF_V8 = OFF_K8 + (KV8 ? S8 * KV8_BYTES : 0);
+  static constexpr uint32_t OFF_BAR = OFF_V8 + (KV8 ? S8 * KV8_BYTES : 0);
   static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
   // TMEM: tile t owns columns [t * TILE_COLS, +BN) for S (P over it) and
   // [t * TILE_COLS + BN, +D) for O.
@@ -74,16 +82,28 @@ struct Tc2Cfg {
       B_PF = B_SF + 2,                          // [2] P_t written (128 arrivals)
       B_OF = B_PF + 2,                          // [2] O_t += P_t V done
       B_Q = B_OF + 2,                           // [2] Q_t staged (128 arrivals)
-      B_DRAIN = B_Q + 2, NBAR = B_DRAIN + 1;
+      B_DRAIN = B_Q + 2,                        // every MMA done
+      B_K8F = B_DRAIN + 1, B_K8E = B_K8F + S8,  // fp8 code rings: full / empty
+      B_V8F = B_K8E + S8, B_V8E = B_V8F + S8, NBAR = B_V8E + S8;
   static_assert(2 * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NBAR * 8 <= 240, "barrier area");
+  static_assert(!KV8 || D == 128, "fp8 caches: one 128-byte TMA box per key row");
 };
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -101,16 +121,17 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
 }
 
-template <typename T, int D>
+template <typename T, int D, bool KV8>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc2_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
-  using C = Tc2Cfg<D>;
+  using C = Tc2Cfg<D, KV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sK8 = base + C::OFF_K8, sV8 = base + C::OFF_V8;
   const uint32_t bar0 = base + C::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
@@ -148,12 +169,13 @@ __global__ void __launch_bounds__(384, 1)
 
   // ---- barriers and TMEM ----------------------------------------------------
   if (threadIdx.x == 0) {
+    // fp8 caches: the 16-bit stages are filled by the two widening warps
     for (int s = 0; s < C::KS; ++s) {
-      mbar_init(bar(C::B_KF + s), 1);
+      mbar_init(bar(C::B_KF + s), KV8 ? 2 : 1);
       mbar_init(bar(C::B_KE + s), 1);
     }
     for (int s = 0; s < C::VS; ++s) {
-      mbar_init(bar(C::B_VF + s), 1);
+      mbar_init(bar(C::B_VF + s), KV8 ? 2 : 1);
       mbar_init(bar(C::B_VE + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -163,6 +185,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_Q + t), 128);
     }
     mbar_init(bar(C::B_DRAIN), 1);
+    for (int s = 0; s < C::S8; ++s) {
+      mbar_init(bar(C::B_K8F + s), 1);
+      mbar_init(bar(C::B_K8E + s), 2);
+      mbar_init(bar(C::B_V8F + s), 1);
+      mbar_init(bar(C::B_V8E + s), 2);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -177,7 +205,136 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp < 4) {
     setmaxnreg_dec<REG_LOW>();
-    if (warp == 0 || warp == 2) {
+    if (KV8 && warp == 0) {
+      // ===== fp8 cache: warp 0 streams the K and V codes of each key tile ======
+      // into the code rings, one TMA box (16 keys x 128 codes) per page slot;
+      // the slot holding the row's last key is copied by hand, zero-filled.
+      const uint8_t* kc8 = static_cast<const uint8_t*>(a.kc);
+      const uint8_t* vc8 = static_cast<const uint8_t*>(a.vc);
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
+      const int P = p.page_size;
+      const int64_t bt_row = (int64_t)b * p.max_pages;
+      int j = 0;
+      bool ok = true;
+      for (; j < n_kv; ++j) {
+        const int st = j % C::S8;
+        const int kbase = j * C::BN;
+        int kind = 0, tok0 = 0;
+        if (lane < C::SLOTS) {
+          const int s0 = kbase + 16 * lane;
+          if (s0 >= L) {
+            kind = 3;
+          } else {
+            const int col = s0 / P;
+            const int page = col < p.max_pages ? __ldg(p.bt + bt_row + col) : -1;
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+              kind = 3;
+            } else {
+              tok0 = page * P + (s0 % P);
+              kind = (s0 + 16 <= L) ? 1 : 2;
+            }
+          }
+        }
+        const uint32_t manual_all = __ballot_sync(0xffffffffu, kind >= 2);
+        const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          if (j >= C::S8)
+            ok = mbar_wait(bar((kv ? C::B_V8E : C::B_K8E) + st), ((j / C::S8) - 1) & 1, abort_flag,
+                           p.err);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = (kv ? sV8 : sK8) + st * C::KV8_BYTES;
+          const uint8_t* cache = kv ? vc8 : kc8;
+          uint32_t manual = manual_all;
+          while (manual) {
+            const int s = __ffs(manual) - 1;
+            manual &= manual - 1;
+            const int ks = __shfl_sync(0xffffffffu, kind, s);
+            const int t0 = __shfl_sync(0xffffffffu, tok0, s);
+            const int nvalid = ks == 2 ? L - (kbase + 16 * s) : 0;
+            for (int it = lane; it < 16 * 8; it += 32) {
+              const int unit = it & 7, rr = it >> 3;
+              uint4 v = make_uint4(0u, 0u, 0u, 0u);
+              if (rr < nvalid)
+                v = __ldg(reinterpret_cast<const uint4*>(
+                    cache + ((int64_t)(t0 + rr) * p.hkv + kh) * D + unit * 16));
+              const int row = 16 * s + rr;
+              st_shared_v4(dst + row * 128 + ((unit ^ (row & 7)) << 4), v);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t fb = bar((kv ? C::B_V8F : C::B_K8F) + st);
+          if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_tma * 16u * 128u);
+          __syncwarp();
+          if (kind == 1) tma_load_3d(dst + lane * 16 * 128, kv ? (const void*)&tmV : (const void*)&tmK, 0, kh, tok0, fb);
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        // copies this warp started may still be landing: wait for them
+        for (int jj = max(0, j - C::S8); jj <= j && jj < n_kv; ++jj) {
+          mbar_drain(bar(C::B_K8F + jj % C::S8), (jj / C::S8) & 1, p.err);
+          if (jj < j) mbar_drain(bar(C::B_V8F + jj % C::S8), (jj / C::S8) & 1, p.err);
+        }
+      }
+    } else if (KV8 && (warp == 2 || warp == 3)) {
+      // ===== fp8 cache: warps 2 and 3 widen every K and V tile =================
+      // (keys [64 (warp - 2), +64) each) into the 16-bit swizzled tiles the
+      // MMAs read.  An E5M2 code in the high byte of a binary16 is the same
+      // value (exact); for bf16 Q it is widened through fp32, also exactly.
+      // Lane = 16 codes of one key per step.
+      const int key0 = 64 * (warp - 2);
+      const int u = lane & 7, c = u >> 2, va = 2 * (u & 3);
+      auto widen = [&](uint32_t src, uint32_t dst) {
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int key = key0 + 4 * it + (lane >> 3);
+          const uint4 w = ld_shared_v4(src + key * 128 + ((u ^ (key & 7)) << 4));
+          uint4 lo, hi;
+          e5m2x4_to<T>(w.x, lo.x, lo.y);
+          e5m2x4_to<T>(w.y, lo.z, lo.w);
+          e5m2x4_to<T>(w.z, hi.x, hi.y);
+          e5m2x4_to<T>(w.w, hi.z, hi.w);
+          const uint32_t row = dst + c * (C::BN * 128) + key * 128;
+          st_shared_v4(row + ((va ^ (key & 7)) << 4), lo);
+          st_shared_v4(row + (((va + 1) ^ (key & 7)) << 4), hi);
+        }
+        // the MMAs read the tile through the async proxy; TMA overwrites the
+        // codes next
+        fence_proxy_async_smem();
+        __syncwarp();
+      };
+      bool ok = true;
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st8 = j % C::S8;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+          const int NS = kv ? C::VS : C::KS, st = j % NS;
+          ok = ok && mbar_wait(bar((kv ? C::B_V8F : C::B_K8F) + st8), (j / C::S8) & 1, abort_flag,
+                               p.err);
+          if (ok && j >= NS)
+            ok = mbar_wait(bar((kv ? C::B_VE : C::B_KE) + st), ((j / NS) - 1) & 1, abort_flag,
+                           p.err);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          widen((kv ? sV8 : sK8) + st8 * C::KV8_BYTES, (kv ? sV : sK) + st * C::KV_BYTES);
+          if (lane == 0) {
+            mbar_arrive(bar((kv ? C::B_VF : C::B_KF) + st));
+            mbar_arrive(bar((kv ? C::B_V8E : C::B_K8E) + st8));
+          }
+        }
+      }
+    } else if (!KV8 && (warp == 0 || warp == 2)) {
       // ============ producers: warp 0 streams K tiles, warp 2 V tiles ========
       const bool isK = warp == 0;
       const int NS = isK ? C::KS : C::VS;
@@ -473,11 +630,11 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool KV8>
 cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
                        cudaStream_t st) {
-  using C = Tc2Cfg<D>;
-  auto k = prefill_tc2_kernel<T, D>;
+  using C = Tc2Cfg<D, KV8>;
+  auto k = prefill_tc2_kernel<T, D, KV8>;
   static DeviceFlags attr;
   cudaError_t e = attr.once([&] {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -487,14 +644,14 @@ cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& tk, const CUtensorM
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool KV8>
 bool regs_ok() {
   // the register split is only safe when the kernel launches with exactly
   // REG_LAUNCH registers per thread
   static int ok = -1;
   if (ok < 0) {
     cudaFuncAttributes fa{};
-    ok = cudaFuncGetAttributes(&fa, prefill_tc2_kernel<T, D>) == cudaSuccess &&
+    ok = cudaFuncGetAttributes(&fa, prefill_tc2_kernel<T, D, KV8>) == cudaSuccess &&
          fa.numRegs == REG_LAUNCH;
   }
   return ok == 1;
@@ -503,27 +660,35 @@ bool regs_ok() {
 }  // namespace
 
 bool prefill_tc2_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
-  if (!((q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype && (d == 64 || d == 128) &&
-        cache_tokens < (int64_t(1) << 31)))
+  if (!(q_dtype == PA_BF16 || q_dtype == PA_F16) || cache_tokens >= (int64_t(1) << 31))
     return false;
   const bool bf = q_dtype == PA_BF16;
-  if (d == 64) return bf ? regs_ok<__nv_bfloat16, 64>() : regs_ok<__half, 64>();
-  return bf ? regs_ok<__nv_bfloat16, 128>() : regs_ok<__half, 128>();
+  if (kv_dtype == PA_E5M2 && d == 128)
+    return bf ? regs_ok<__nv_bfloat16, 128, true>() : regs_ok<__half, 128, true>();
+  if (kv_dtype != q_dtype || !(d == 64 || d == 128)) return false;
+  if (d == 64) return bf ? regs_ok<__nv_bfloat16, 64, false>() : regs_ok<__half, 64, false>();
+  return bf ? regs_ok<__nv_bfloat16, 128, false>() : regs_ok<__half, 128, false>();
 }
 
-cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st) {
+cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int grid_x,
+                               cudaStream_t st) {
   if (grid_x == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;
-  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+  if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
   const bool bf = q_dtype == PA_BF16;
+  if (kv_dtype == PA_E5M2) {
+    if (a.p.d != 128) return cudaErrorInvalidValue;
+    return bf ? launch_tc2<__nv_bfloat16, 128, true>(a, tk, tv, grid_x, st)
+              : launch_tc2<__half, 128, true>(a, tk, tv, grid_x, st);
+  }
   switch (a.p.d) {
-    case 64: return bf ? launch_tc2<__nv_bfloat16, 64>(a, tk, tv, grid_x, st)
-                       : launch_tc2<__half, 64>(a, tk, tv, grid_x, st);
-    case 128: return bf ? launch_tc2<__nv_bfloat16, 128>(a, tk, tv, grid_x, st)
-                        : launch_tc2<__half, 128>(a, tk, tv, grid_x, st);
+    case 64: return bf ? launch_tc2<__nv_bfloat16, 64, false>(a, tk, tv, grid_x, st)
+                       : launch_tc2<__half, 64, false>(a, tk, tv, grid_x, st);
+    case 128: return bf ? launch_tc2<__nv_bfloat16, 128, false>(a, tk, tv, grid_x, st)
+                        : launch_tc2<__half, 128, false>(a, tk, tv, grid_x, st);
   }
   return cudaErrorInvalidValue;
 }

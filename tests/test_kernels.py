@@ -85,6 +85,24 @@ def test_prefill_small(dtype, d, hq, hkv):
     assert max_err(out, ref_of(cpu)) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_prefill_fp8_cache(dtype, d):
+    # E5M2 K/V with per-tensor scales on the prefill path: ragged rows (a
+    # partial last page slot, q > L, several 128-key tiles), page-size
+    # invariance bitwise, NaN poison in unused slots never reaching the output
+    ql, kl = [65, 300, 3, 129, 40], [65, 1500, 1, 700, 33]
+    outs = {}
+    for P in (16, 48):
+        cpu, gpu = small(ql, kl, hq=8, hkv=2, d=d, P=P, dtype=dtype, kv_dtype="e5m2",
+                         seed=5 + d, k_scale=0.37, v_scale=1.7,
+                         poison="nan" if P == 48 else "finite")
+        outs[P] = run("prefill", gpu)
+        if P == 16:
+            assert max_err(outs[P], ref_of(cpu)) <= TOL["e5m2"]
+    assert_bitwise(outs[48], outs[16])
+
+
 DECODE_LENS = [0, 1, 31, 32, 33, 511, 512, 513, 4097, 10000]
 
 
