@@ -278,6 +278,29 @@ def part_mixed3(steps, warmup, stream, pk):
     return res
 
 
+def part_prefill_fp8(steps, warmup, stream, pk):
+    """The varlen prefill workload's shapes with fp16 Q and an fp8 E5M2 cache
+    (per-tensor scales 0.5 / 2.0): the prefill path's fp8 dequant."""
+    import paged_kv_attention_prefill_gb300 as pa
+    b = workloads.make_workload(2, device="cuda", data_device="cuda", q_dtype="f16",
+                                kv_dtype="e5m2", k_scale=0.5, v_scale=2.0)
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+
+    def fn():
+        pa.paged_attn_prefill(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                              b.seq_lens, out=out, workspace=ws, **kw)
+    ms = time_calls(fn, steps, warmup, stream)
+    F = metrics.prefill_flops(b.q_lens, b.kv_lens, b.num_q_heads, b.head_dim)
+    tf = F / (ms * 1e-3) / 1e12
+    res = {"workload": workloads.WORKLOADS[2] + ", with fp16 Q and an fp8_e5m2 KV cache",
+           "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_of_fp16_peak": round(tf / pk["bf16"], 4)}
+    del b, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def part_small1(steps, warmup, stream):
     import paged_kv_attention_prefill_gb300 as pa
     b = workloads.make_workload(1).to("cuda")
@@ -426,6 +449,7 @@ def run_ours(args):
             parts["decode_split_kv_256rows"] = part_decode(4, ps, pw, stream, pk)
             parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk)
             parts["mixed_chunk_plus_decode"] = part_mixed3(ps, pw, stream, pk)
+            parts["prefill_fp8_cache"] = part_prefill_fp8(ps, pw, stream, pk)
             parts["decode_small_4rows"] = part_small1(max(ps, 50), 5, stream)
         cpu_val, cores, sample, cpu_extra = cpu_baseline_sample(b, budget_s=args.cpu_seconds)
         res = {
