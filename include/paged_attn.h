@@ -121,7 +121,26 @@ typedef struct pa_params {
                              split-KV decode path; 0 selects 16.  decode: the
                              largest q_b allowed. */
   int32_t num_splits;     /* split-KV parts per decode row: 0 or 16 */
+  int32_t verify_mode;    /* decode rows with q_b > 1: PA_VERIFY_PACKED (0) or
+                             PA_VERIFY_TOKENWISE (1), see below */
 } pa_params;
+
+/*
+ * Decode rows with q_b > 1 (speculative-verify rows):
+ *  PA_VERIFY_PACKED     the row's q_b * g query rows share one pass over the
+ *                       row's keys, split by the row's L_b (K/V read once).
+ *  PA_VERIFY_TOKENWISE  token i of the row is computed as a decode row of its
+ *                       own, q = 1 over the first L_b - q_b + 1 + i keys and
+ *                       split by that length: each token's result is bitwise
+ *                       equal to decoding the tokens one at a time (1Cat-vLLM
+ *                       PR #616, "Purpose": a verify row expanded into single
+ *                       tokens; vllm-rlt PR #128, "Purpose": packed rows equal
+ *                       serial decode only where the kernel makes them so).
+ *                       The row's K/V is read once per token.  Supported for
+ *                       16-bit q (same-type or E5M2 caches); other dtypes
+ *                       return PA_ERR_UNSUPPORTED.
+ */
+enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
 
 typedef struct pa_batch {
   int32_t num_rows;             /* B >= 0 */

@@ -50,7 +50,9 @@ class Params(ctypes.Structure):
                 ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("max_decode_q", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("verify_mode", ctypes.c_int32)]
+
+PA_VERIFY_PACKED, PA_VERIFY_TOKENWISE = 0, 1
 
 
 class Batch(ctypes.Structure):
@@ -110,11 +112,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_params(q, k_cache, *, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-                num_splits=0) -> Params:
+                num_splits=0, verify_mode=PA_VERIFY_PACKED) -> Params:
     return Params(int(q.shape[1]), int(k_cache.shape[2]), int(q.shape[2]),
                   int(k_cache.shape[1]), _dtype_code(q), _dtype_code(k_cache),
                   float(softmax_scale or 0.0), float(k_scale), float(v_scale),
-                  int(max_decode_q), int(num_splits))
+                  int(max_decode_q), int(num_splits), int(verify_mode))
 
 
 def workspace_size(params: Params, num_rows: int, total_q: int) -> int:
@@ -142,7 +144,8 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out=None,
           workspace=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-          cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
+          verify_mode=PA_VERIFY_PACKED, cu_seqlens_q_host=None, seq_lens_host=None,
+          stream=None):
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         if not t.is_cuda:
             raise PagedAttnError("all tensors must be CUDA tensors")
@@ -152,7 +155,7 @@ def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out
             seq_lens.dtype != torch.int32:
         raise PagedAttnError("block_table, cu_seqlens_q and seq_lens must be int32")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
-                      v_scale=v_scale, max_decode_q=max_decode_q)
+                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode)
     B = int(seq_lens.shape[0])
     total_q = int(q.shape[0])
     if out is None:
@@ -196,8 +199,8 @@ def paged_attn_mixed(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *
 
 def paged_attn_decode_static(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *,
                              out=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0,
-                             max_decode_q=0, cu_seqlens_q_host=None, seq_lens_host=None,
-                             stream=None):
+                             max_decode_q=0, verify_mode=PA_VERIFY_PACKED,
+                             cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
     """Split-KV decode without a workspace: for callers that cannot allocate
     device memory.  The library's fixed device array (STATIC_SCRATCH_BYTES,
     shared by every call) holds the scratch; larger batches are refused.
@@ -206,7 +209,7 @@ def paged_attn_decode_static(q, k_cache, v_cache, block_table, cu_seqlens_q, seq
         if not t.is_cuda or not t.is_contiguous():
             raise PagedAttnError("all tensors must be contiguous CUDA tensors")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
-                      v_scale=v_scale, max_decode_q=max_decode_q)
+                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode)
     B = int(seq_lens.shape[0])
     if out is None:
         out = torch.empty_like(q)

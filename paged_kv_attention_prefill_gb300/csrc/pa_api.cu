@@ -42,6 +42,7 @@ struct Resolved {
   int qd, kvd;
   float scale, k_scale, v_scale;
   int max_dq;
+  int tokenwise;      // decode rows with q_b > 1 as one-token rows
   bool host;          // host mirrors present
   int host_max_q_dec; // mixed/decode: largest q_b among decode rows (host mirrors)
   int host_tiles;     // prefill work items (host mirrors), for the tile height in use
@@ -98,6 +99,9 @@ pa_status resolve_params(const pa_params* prm, Resolved* r) {
   r->k_scale = prm->k_scale != 0.f ? prm->k_scale : 1.f;
   r->v_scale = prm->v_scale != 0.f ? prm->v_scale : 1.f;
   r->max_dq = prm->max_decode_q ? prm->max_decode_q : 16;
+  if (prm->verify_mode != PA_VERIFY_PACKED && prm->verify_mode != PA_VERIFY_TOKENWISE)
+    return PA_ERR_INVALID_ARG;
+  r->tokenwise = prm->verify_mode == PA_VERIFY_TOKENWISE;
   return PA_OK;
 }
 
@@ -125,6 +129,9 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   const int64_t cache_tokens = (int64_t)bat->num_pages * r->P;
   r->tc2 = prefill_tc2_supported(r->qd, r->kvd, r->d, cache_tokens);
   r->tc = !r->tc2 && prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens);
+  // one-token verify rows run on the TMA decode kernel only
+  if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
+    return PA_ERR_UNSUPPORTED;
   r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
   r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
   r->host_max_q_dec = 0;
@@ -187,6 +194,8 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.n_tiles = &reinterpret_cast<const WsHeader*>(base)->n_tiles;
   a.max_decode_q = r.max_dq;
   a.max_slots = w.max_slots;
+  a.tokenwise = r.tokenwise;
+  a.n_slots = nullptr;
   return a;
 }
 
@@ -226,7 +235,8 @@ AuxStream* aux_stream() {
 }
 
 int decode_mblocks(const Resolved& r, int max_q) {
-  return (max_q * r.g + DEC_ROWS - 1) / DEC_ROWS;
+  // tokenwise verify rows: one token's g query rows per work item
+  return ((r.tokenwise ? 1 : max_q) * r.g + DEC_ROWS - 1) / DEC_ROWS;
 }
 
 // Launches the decode CTAs and the merge for the rows routed to decode.
@@ -243,12 +253,16 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
   if (r.qd == PA_F32)
     e = launch_f32(a, 1, 0, n_mblk, st);
   else if (decode_tma_supported(r.qd, r.kvd, r.d, (int64_t)a.p.num_pages * a.p.page_size)) {
-    if (order && a.p.num_rows >= ORDER_MIN_ROWS && a.p.num_rows <= MAX_ORDER_ROWS) {
+    if (!r.tokenwise && order && a.p.num_rows >= ORDER_MIN_ROWS &&
+        a.p.num_rows <= MAX_ORDER_ROWS) {
       e = launch_row_order(a, order, st);
       if (e != cudaSuccess) return e;
       a.row_order = order;
     }
-    e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, st);
+    // packed: work items range over rows; tokenwise: over decode slots
+    const int units = r.tokenwise ? (int)std::min<int64_t>(a.p.total_q, a.max_slots)
+                                  : a.p.num_rows;
+    e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, units, st);
   } else
     e = launch_decode_mma(a, r.qd, r.kvd, n_mblk, st);
   if (e != cudaSuccess) return e;
@@ -323,6 +337,7 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   uint8_t* base = static_cast<uint8_t*>(workspace);
   a.dec_base = reinterpret_cast<const int32_t*>(base + w.dec_base);
   a.slot_tok = reinterpret_cast<const int32_t*>(base + w.slot_tok);
+  a.n_slots = &reinterpret_cast<const WsHeader*>(base)->n_slots;
   const int bm = r.pf_bm;
   const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
   cudaError_t e = launch_plan(a, 1, r.max_dq, bm, max_tiles, st);

@@ -201,8 +201,13 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
     const int mid = (lo + hi + 1) >> 1;
     if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
   }
-  const int L = __ldg(p.seq_lens + lo);
-  const int n_tiles = (L + DEC_KT - 1) / DEC_KT;
+  int L = __ldg(p.seq_lens + lo);
+  if (a.tokenwise) {
+    // a one-token row: its own length, so its own partition
+    const int qs = __ldg(p.cu_q + lo), qb = __ldg(p.cu_q + lo + 1) - qs;
+    L = L - qb + 1 + (t - qs);
+  }
+  const int n_tiles = L > 0 ? (L + DEC_KT - 1) / DEC_KT : 0;
   const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
   const int nsp = tps ? (n_tiles + tps - 1) / tps : 0;
 

@@ -140,18 +140,40 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
   f.split = rest % NSPLIT;
   rest /= NSPLIT;
   f.kh = rest % p.hkv;
-  f.b = rest / p.hkv;
-  if (a.row_order) f.b = __ldg(a.row_order + f.b);
-  f.qs = __ldg(p.cu_q + f.b);
-  f.qb = __ldg(p.cu_q + f.b + 1) - f.qs;
-  if (f.qb <= 0 || f.qs < 0 || f.qs + f.qb > p.total_q) return false;
-  f.slot_base = f.qs;
-  if (a.dec_base) {
-    f.slot_base = __ldg(a.dec_base + f.b);
-    if (f.slot_base < 0) return false;
+  if (a.tokenwise) {
+    // one-token rows: unit = decode slot; token i of row b is a row of its
+    // own with q = 1 and L = L_b - q_b + 1 + i
+    const int slot = rest / p.hkv;
+    if (a.n_slots && slot >= (int)*a.n_slots) return false;
+    if (slot >= a.max_slots) return false;
+    const int t = a.slot_tok ? __ldg(a.slot_tok + slot) : slot;
+    if (t < 0 || t >= p.total_q || p.num_rows <= 0) return false;
+    int lo = 0, hi = p.num_rows - 1;  // row of token t: largest b with cu_q[b] <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int qs = __ldg(p.cu_q + lo), qb = __ldg(p.cu_q + lo + 1) - qs;
+    if (t < qs || t >= qs + qb) return false;
+    f.b = lo;
+    f.qs = t;
+    f.qb = 1;
+    f.slot_base = slot;
+    f.L = __ldg(p.seq_lens + lo) - qb + 1 + (t - qs);
+  } else {
+    f.b = rest / p.hkv;
+    if (a.row_order) f.b = __ldg(a.row_order + f.b);
+    f.qs = __ldg(p.cu_q + f.b);
+    f.qb = __ldg(p.cu_q + f.b + 1) - f.qs;
+    if (f.qb <= 0 || f.qs < 0 || f.qs + f.qb > p.total_q) return false;
+    f.slot_base = f.qs;
+    if (a.dec_base) {
+      f.slot_base = __ldg(a.dec_base + f.b);
+      if (f.slot_base < 0) return false;
+    }
+    if ((int64_t)f.slot_base + f.qb > a.max_slots) return false;
+    f.L = __ldg(p.seq_lens + f.b);
   }
-  if ((int64_t)f.slot_base + f.qb > a.max_slots) return false;
-  f.L = __ldg(p.seq_lens + f.b);
   f.M = f.qb * p.g;
   f.r0 = f.mblk * 16;
   if (f.r0 >= f.M) return false;
@@ -645,9 +667,9 @@ bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens
 }
 
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
-                              cudaStream_t st) {
-  if (a.p.num_rows == 0 || n_mblk == 0) return cudaSuccess;
-  const int64_t items = (int64_t)a.p.num_rows * a.p.hkv * NSPLIT * n_mblk;
+                              int n_units, cudaStream_t st) {
+  if (a.p.num_rows == 0 || n_mblk == 0 || n_units <= 0) return cudaSuccess;
+  const int64_t items = (int64_t)n_units * a.p.hkv * NSPLIT * n_mblk;
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;

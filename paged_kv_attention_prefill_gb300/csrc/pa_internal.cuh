@@ -92,7 +92,9 @@ struct AttnArgs {
   const uint32_t* n_tiles;   // its length (device)
   int max_decode_q;
   int64_t max_slots;         // decode slots the workspace holds
-  int dec_mblk;              // decode grid: 16-row query blocks per row
+  int dec_mblk;              // decode grid: 16-row query blocks per row (per token if tokenwise)
+  int tokenwise;             // decode rows with q_b > 1 expanded into one-token rows
+  const uint32_t* n_slots;   // mixed: decode slots in use (device); null: every token is a slot
 };
 
 // Launchers (one per translation unit family).  Return cudaError_t.
@@ -122,8 +124,9 @@ cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int
                                cudaStream_t st);
 // persistent TMA-fed split-KV decode (16-bit q; same-type or fp8 E5M2 cache)
 bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
+// n_units: rows (packed) or decode slots (tokenwise) the work items range over
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
-                              cudaStream_t st);
+                              int n_units, cudaStream_t st);
 bool decode_mma_supported(int q_dtype, int kv_dtype, int d);
 
 // ---------------------------------------------------------------------------

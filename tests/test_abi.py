@@ -116,6 +116,16 @@ def test_rejects_bad_params(lib, name):
 
 
 @pytest.mark.parametrize("name", ENTRIES)
+def test_verify_mode_checks(lib, name):
+    # an unknown verify mode is refused by every entry; one-token verify rows
+    # run on the 16-bit decode kernel only, so fp32 decode/mixed refuse them
+    assert FakeCall(lib, params(verify_mode=7), [1, 1], [10, 20])(name) == INVALID
+    if name != "paged_attn_prefill":
+        p = params(q_dtype=pa.PA_F32, kv_dtype=pa.PA_F32, verify_mode=pa.PA_VERIFY_TOKENWISE)
+        assert FakeCall(lib, p, [1, 1], [10, 20])(name) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("name", ENTRIES)
 def test_rejects_bad_batches(lib, name):
     p = params()
     assert FakeCall(lib, p, [1], [-2])(name) == INVALID                 # negative length

@@ -140,6 +140,54 @@ def test_decode_many_rows_work_order(entry, kv):
         assert_bitwise(out[cu[r]:cu[r + 1]], alone)
 
 
+def _serial_rows(b, rows):
+    """Each token i of each listed row as a q = 1 row of its own over the first
+    L - q + 1 + i keys of the same pages (what decoding the tokens one at a
+    time computes)."""
+    cu = b.cu_seqlens_q.cpu().tolist()
+    L = b.seq_lens.cpu().tolist()
+    bt = b.block_table
+    toks, lens, tabs = [], [], []
+    for r in rows:
+        q = cu[r + 1] - cu[r]
+        for i in range(q):
+            toks.append(cu[r] + i)
+            lens.append(max(0, L[r] - q + 1 + i))
+            tabs.append(bt[r])
+    dev = b.q.device
+    return dict(q=b.q[toks].contiguous(), block_table=torch.stack(tabs).contiguous(),
+                cu_seqlens_q=torch.arange(len(toks) + 1, dtype=torch.int32, device=dev),
+                seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev)), toks
+
+
+@pytest.mark.parametrize("dtype,kv", [("bf16", None), ("f16", "e5m2")])
+def test_verify_rows_tokenwise_equal_serial_decode(dtype, kv):
+    # q > 1 decode rows in one-token mode: every token bitwise equal to a q = 1
+    # decode of its own prefix, through the decode and the mixed entries
+    ql = [1, 4, 5, 16, 3, 2]
+    kl = [300, 700, 129, 2049, 2, 5000]          # row 4: q > L, its first token sees nothing
+    cpu, gpu = small(ql, kl, hq=8, hkv=2, d=128, P=16, dtype=dtype, kv_dtype=kv, seed=41,
+                     k_scale=0.37 if kv else 1.0, v_scale=1.7 if kv else 1.0)
+    tw = run("decode", gpu, verify_mode=pa.PA_VERIFY_TOKENWISE)
+    assert max_err(tw, ref_of(cpu)) <= tol_of(cpu)
+    ser, toks = _serial_rows(gpu, range(len(ql)))
+    serial = pa.paged_attn_decode(ser["q"], gpu.k_cache, gpu.v_cache, ser["block_table"],
+                                  ser["cu_seqlens_q"], ser["seq_lens"],
+                                  softmax_scale=gpu.softmax_scale, k_scale=gpu.k_scale,
+                                  v_scale=gpu.v_scale)
+    torch.cuda.synchronize()
+    assert_bitwise(tw[toks], serial)
+    # the same rows next to a prefill row in a mixed call
+    ql2, kl2 = ql + [100], kl + [900]
+    cpu2, gpu2 = small(ql2, kl2, hq=8, hkv=2, d=128, P=16, dtype=dtype, kv_dtype=kv, seed=41,
+                       k_scale=0.37 if kv else 1.0, v_scale=1.7 if kv else 1.0)
+    mixed = run("mixed", gpu2, verify_mode=pa.PA_VERIFY_TOKENWISE)
+    dec_alone = run("decode", workloads.sub_batch(cpu2, range(len(ql))).to("cuda"),
+                    verify_mode=pa.PA_VERIFY_TOKENWISE)
+    assert_bitwise(mixed[:sum(ql)], dec_alone)
+    assert max_err(mixed, ref_of(cpu2)) <= tol_of(cpu2)
+
+
 @pytest.mark.parametrize("dtype,kv", [("bf16", None), ("f16", "e5m2"), ("f32", None)])
 def test_mixed_small_and_routing_bitwise(dtype, kv):
     ql = [300, 1, 4, 0, 17, 16, 2]
