@@ -50,10 +50,10 @@ L2_BYTES = 129 * 1024 * 1024
 # Reported only while the kernel's sources are the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "be9d5d1d4e7436341782b95b8ce43f20a125248f09c0dfc67f60f02d82ff71b3",
-        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "f3adf47265b0acda2025bac2ca22fb1aaeddec86e8d55801cc41b513356c6166",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "9a0a4840221133f584833e6de02e98c05e199363e7a33a7901bec63d25ce79de",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "b118652fb223ae088defcdb22930b457bfd73b3d16884163b65a6288e74fcdb2",
     },
-    "bytes_per_launch": 959060480 + 54701312,
+    "bytes_per_launch": 956704000 + 55211008,
 }
 
 
