@@ -420,25 +420,68 @@ def run_ours(args):
     value = total_flops / (ms * 1e-3) / 1e12
     achieved = F / (ms_local * 1e-3) / 1e12
 
-    # end to end through the public API with host buffers
-    in_bytes = sum(t.numel() * t.element_size() for t in
-                   (b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens))
-    host = {k: getattr(b, k).cpu().pin_memory() for k in
-            ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seq_lens")}
-    dev = {k: torch.empty_like(getattr(b, k)) for k in host}
-    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    # end to end through the public API with host buffers, fed the way a
+    # serving loop feeds it: step i+1's inputs are copied host -> device (two
+    # copy streams, the K cache on one, everything else on the other) into a
+    # second set of device buffers while step i computes, and step i's output
+    # is copied back behind it.  Every step's copies are inside the timed
+    # region, which runs from before the first upload to after the last
+    # download.
+    names = ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seq_lens")
+    in_bytes = sum(getattr(b, k).numel() * getattr(b, k).element_size() for k in names)
+    host = {k: getattr(b, k).cpu().pin_memory() for k in names}
+    dev = [{k: torch.empty_like(getattr(b, k)) for k in names} for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    out_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    copy_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    groups = (("k_cache",), ("v_cache", "q", "block_table", "cu_seqlens_q", "seq_lens"))
 
-    def e2e_step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        pa.paged_attn_mixed(dev["q"], dev["k_cache"], dev["v_cache"], dev["block_table"],
-                            dev["cu_seqlens_q"], dev["seq_lens"], out=out, workspace=ws, **kw)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_run(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ready = [[torch.cuda.Event(), torch.cuda.Event()] for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        back = [torch.cuda.Event() for _ in range(n)]
+        start.record(stream)
+
+        def upload(i):
+            for c, keys, ev in zip(copy_streams, groups, ready[i]):
+                c.wait_event(start)
+                if i >= 2:
+                    c.wait_event(done[i - 2])  # the buffer set is free again
+                with torch.cuda.stream(c):
+                    for k in keys:
+                        dev[i % 2][k].copy_(host[k], non_blocking=True)
+                ev.record(c)
+
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            for ev in ready[i]:
+                stream.wait_event(ev)
+            if i >= 2:
+                stream.wait_event(back[i - 2])  # the output buffer is free again
+            d = dev[i % 2]
+            pa.paged_attn_mixed(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                d["cu_seqlens_q"], d["seq_lens"], out=outs[i % 2], workspace=ws,
+                                **kw)
+            done[i].record(stream)
+            c = copy_streams[1]
+            c.wait_event(done[i])
+            with torch.cuda.stream(c):
+                out_host[i % 2].copy_(outs[i % 2], non_blocking=True)
+            back[i].record(c)
+        stream.wait_event(back[n - 1])
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / n
 
     e2e_steps = max(3, min(args.steps, 20))
-    ms_e2e = padist.max_over_ranks(time_calls(e2e_step, e2e_steps, 2, stream), device="cuda")
+    e2e_run(2)  # warm-up
+    padist.barrier()
+    ms_e2e = padist.max_over_ranks(e2e_run(e2e_steps), device="cuda")
     e2e_val = total_flops / (ms_e2e * 1e-3) / 1e12
-    del host, dev
+    del host, dev, outs, out_host
     torch.cuda.empty_cache()
 
     res = None
@@ -471,7 +514,10 @@ def run_ours(args):
                              "kind": "oracle", "sample": sample, **cpu_extra},
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 3),
                     "h2d_bytes_per_step": in_bytes,
-                    "d2h_bytes_per_step": out.numel() * out.element_size()},
+                    "d2h_bytes_per_step": out.numel() * out.element_size(),
+                    "steps": e2e_steps,
+                    "how": "pinned host buffers; step i+1's uploads (two copy streams) overlap "
+                           "step i's compute, each step's download follows it"},
             "gpu_launches": launches_per_call(ql) * args.steps,
             "clocks": clocks,
             "parts": parts,
