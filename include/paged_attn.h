@@ -123,6 +123,9 @@ typedef struct pa_params {
   int32_t num_splits;     /* split-KV parts per decode row: 0 or 16 */
   int32_t verify_mode;    /* decode rows with q_b > 1: PA_VERIFY_PACKED (0) or
                              PA_VERIFY_TOKENWISE (1), see below */
+  int32_t prefill_kv_parts; /* prefill work items cut into key-range parts:
+                               0 or 1 = not cut, 2..16 = at most this many
+                               parts, see below */
 } pa_params;
 
 /*
@@ -141,6 +144,26 @@ typedef struct pa_params {
  *                       return PA_ERR_UNSUPPORTED.
  */
 enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
+
+/*
+ * Prefill key-range parts (prefill_kv_parts = K in 2..16; 1Cat-vLLM PR #1279,
+ * commit 5: a CTA's key range split into whole-tile ranges merged by
+ * log-sum-exp).  A prefill work item (a block of GQA-packed query rows of one
+ * row and KV head) whose rows see k_end keys runs as
+ *     parts = min(K, ceil(ceil(k_end / 128) / 128))
+ * CTAs, each over an equal run of whole 128-key units (the last one takes the
+ * rest), chosen from k_end alone; each part writes an fp32 partial state
+ * (acc[d], m, l) per query token and head, and a merge kernel combines the
+ * parts in fixed order.  Items with at most 16384 keys are not cut.  The
+ * work list runs longest part first, so long rows fill the GPU in many
+ * short waves instead of a few long ones.  Results stay deterministic, and
+ * independent of the rest of the batch, the page size and the physical
+ * pages; a cut item equals the uncut one to rounding only.  Applies to the
+ * tcgen05 prefill (16-bit q with a same-type cache, or an E5M2 cache at
+ * head_dim 128); other prefill paths ignore it.  The workspace grows by
+ * total_q * Hq * K * (head_dim + 2) * 4 bytes; paged_attn_decode ignores the
+ * field.  Values outside 0..16 return PA_ERR_INVALID_ARG.
+ */
 
 typedef struct pa_batch {
   int32_t num_rows;             /* B >= 0 */
@@ -161,7 +184,9 @@ typedef struct pa_batch {
  * flags, work counts), the mixed call's row plan, and the fp32 split-KV
  * partial states, (acc[d], m, l) per decode token, query head and split --
  * the vllm-rlt PR #128 "Memory" figure of heads x 16 x (head_dim + 2) x 4
- * bytes per decode token.  Returns 0 for invalid parameters.
+ * bytes per decode token -- plus, with prefill_kv_parts = K > 1, the prefill
+ * parts' states (K per query token and head).  Returns 0 for invalid
+ * parameters.
  * The workspace must be zero-filled once before its first use (the header's
  * error word is sticky); the calls never require it to be zeroed again.
  */

@@ -50,7 +50,8 @@ class Params(ctypes.Structure):
                 ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_float), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("max_decode_q", ctypes.c_int32),
-                ("num_splits", ctypes.c_int32), ("verify_mode", ctypes.c_int32)]
+                ("num_splits", ctypes.c_int32), ("verify_mode", ctypes.c_int32),
+                ("prefill_kv_parts", ctypes.c_int32)]
 
 PA_VERIFY_PACKED, PA_VERIFY_TOKENWISE = 0, 1
 
@@ -112,11 +113,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_params(q, k_cache, *, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-                num_splits=0, verify_mode=PA_VERIFY_PACKED) -> Params:
+                num_splits=0, verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0) -> Params:
     return Params(int(q.shape[1]), int(k_cache.shape[2]), int(q.shape[2]),
                   int(k_cache.shape[1]), _dtype_code(q), _dtype_code(k_cache),
                   float(softmax_scale or 0.0), float(k_scale), float(v_scale),
-                  int(max_decode_q), int(num_splits), int(verify_mode))
+                  int(max_decode_q), int(num_splits), int(verify_mode), int(prefill_kv_parts))
 
 
 def workspace_size(params: Params, num_rows: int, total_q: int) -> int:
@@ -144,8 +145,8 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out=None,
           workspace=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-          verify_mode=PA_VERIFY_PACKED, cu_seqlens_q_host=None, seq_lens_host=None,
-          stream=None):
+          verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0, cu_seqlens_q_host=None,
+          seq_lens_host=None, stream=None):
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         if not t.is_cuda:
             raise PagedAttnError("all tensors must be CUDA tensors")
@@ -155,7 +156,8 @@ def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out
             seq_lens.dtype != torch.int32:
         raise PagedAttnError("block_table, cu_seqlens_q and seq_lens must be int32")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
-                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode)
+                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode,
+                      prefill_kv_parts=prefill_kv_parts)
     B = int(seq_lens.shape[0])
     total_q = int(q.shape[0])
     if out is None:

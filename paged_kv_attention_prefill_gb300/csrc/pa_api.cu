@@ -10,14 +10,16 @@ namespace pa {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-static int64_t max_tiles_for(int num_rows, int total_q, int g, int bm) {
-  return ((int64_t)total_q * g + bm - 1) / bm + num_rows;
+static int64_t max_tiles_for(int num_rows, int total_q, int g, int bm, int pf_parts) {
+  return (((int64_t)total_q * g + bm - 1) / bm + num_rows) * std::max(1, pf_parts);
 }
 
-WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g) {
+WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g,
+                          int pf_parts) {
   WsLayout w{};
   w.max_slots = std::min<int64_t>(total_q, (int64_t)num_rows * max_decode_q);
-  w.max_tiles = max_tiles_for(num_rows, total_q, g, 16);  // the smallest tile height in use
+  // the smallest tile height in use
+  w.max_tiles = max_tiles_for(num_rows, total_q, g, 16, pf_parts);
   size_t off = sizeof(WsHeader);
   w.dec_base = off;
   off += align_up((size_t)num_rows * 4, 256);
@@ -30,7 +32,12 @@ WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_deco
   w.part_ml = off;
   off += align_up((size_t)w.max_slots * hq * NSPLIT * 8, 256);
   w.part_acc = off;
-  off += (size_t)w.max_slots * hq * NSPLIT * d * 4;
+  off += align_up((size_t)w.max_slots * hq * NSPLIT * d * 4, 256);
+  const size_t pf = pf_parts > 1 ? (size_t)total_q * hq * pf_parts : 0;
+  w.pf_ml = off;
+  off += align_up(pf * 8, 256);
+  w.pf_acc = off;
+  off += pf * d * 4;
   w.total = align_up(off, 256);
   return w;
 }
@@ -50,6 +57,8 @@ struct Resolved {
   bool tc;            // prefill on the tcgen05 kernel
   bool tc2;           // prefill on the two-tile tcgen05 kernel
   int pf_bm;          // query rows per prefill work item
+  int pf_parts;       // prefill_kv_parts as given (workspace layout)
+  int pf_cut;         // key-range parts in use (the tcgen05 kernels cut; others do not)
 };
 
 // 0 = not checked, 1 = sm_103, 2 = other
@@ -102,6 +111,9 @@ pa_status resolve_params(const pa_params* prm, Resolved* r) {
   if (prm->verify_mode != PA_VERIFY_PACKED && prm->verify_mode != PA_VERIFY_TOKENWISE)
     return PA_ERR_INVALID_ARG;
   r->tokenwise = prm->verify_mode == PA_VERIFY_TOKENWISE;
+  if (prm->prefill_kv_parts < 0 || prm->prefill_kv_parts > PF_MAX_PARTS) return PA_ERR_INVALID_ARG;
+  r->pf_parts = prm->prefill_kv_parts;
+  r->pf_cut = 0;
   return PA_OK;
 }
 
@@ -112,6 +124,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
                    Resolved* r) {
   pa_status s = resolve_params(prm, r);
   if (s != PA_OK) return s;
+  if (entry == E_DECODE) r->pf_parts = 0;  // no prefill work: no part states
   if (!bat || bat->num_rows < 0 || bat->total_q < 0 || bat->num_pages < 0 ||
       bat->max_pages_per_row < 0)
     return PA_ERR_INVALID_ARG;
@@ -123,7 +136,8 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   if (bat->total_q > 0 && (!q || !out)) return PA_ERR_INVALID_ARG;
   if (bat->num_rows > 0 && (!kc || !vc)) return PA_ERR_INVALID_ARG;
   if ((int64_t)bat->total_q * r->g > INT32_MAX / 2) return PA_ERR_INVALID_ARG;
-  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g);
+  const WsLayout w =
+      workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g, r->pf_parts);
   if (ws_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int64_t cache_tokens = (int64_t)bat->num_pages * r->P;
@@ -133,6 +147,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
     return PA_ERR_UNSUPPORTED;
   r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
+  r->pf_cut = (r->tc2 || r->tc) && r->pf_parts > 1 ? r->pf_parts : 0;
   r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
   r->host_max_q_dec = 0;
   r->host_tiles = 0;
@@ -154,7 +169,17 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
         r->host_max_q_dec = std::max(r->host_max_q_dec, qb);
         r->host_slots += qb;
       } else if (qb > 0) {
-        r->host_tiles += (qb * r->g + bm - 1) / bm;
+        const int nmb = (qb * r->g + bm - 1) / bm;
+        if (r->pf_cut > 1) {
+          for (int m = 0; m < nmb; ++m) {
+            const int r_last = std::min((m + 1) * bm, qb * r->g) - 1;
+            int per;
+            r->host_tiles += std::max(
+                1, pf_part_count(std::min(L, L - qb + r_last / r->g + 1), r->pf_cut, &per));
+          }
+        } else {
+          r->host_tiles += nmb;
+        }
       }
     }
   }
@@ -163,7 +188,8 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
 
 AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const void* kc,
                    const void* vc, void* out, void* ws) {
-  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g);
+  const WsLayout w =
+      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts);
   uint8_t* base = static_cast<uint8_t*>(ws);
   AttnArgs a{};
   a.p.cu_q = bat->cu_seqlens_q;
@@ -196,11 +222,15 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.max_slots = w.max_slots;
   a.tokenwise = r.tokenwise;
   a.n_slots = nullptr;
+  a.pf_parts = r.pf_cut;
+  a.pf_ml = reinterpret_cast<float2*>(base + w.pf_ml);
+  a.pf_acc = reinterpret_cast<float*>(base + w.pf_acc);
   return a;
 }
 
 int32_t* row_order_of(void* ws, const pa_batch* bat, const Resolved& r) {
-  const WsLayout w = workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g);
+  const WsLayout w =
+      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts);
   return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + w.row_order);
 }
 
@@ -269,11 +299,20 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
   return launch_merge(a, r.qd, n_slots, st);
 }
 
-cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, cudaStream_t st) {
+// The prefill kernel over the work list, then (when work items were cut into
+// key-range parts) the merge of the parts.
+cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, int mixed,
+                        cudaStream_t st) {
   if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
-  if (r.tc2) return launch_prefill_tc2(a, r.qd, r.kvd, grid_tiles, st);
-  if (r.tc) return launch_prefill_tc(a, r.qd, grid_tiles, st);
-  return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
+  cudaError_t e;
+  if (r.tc2)
+    e = launch_prefill_tc2(a, r.qd, r.kvd, grid_tiles, st);
+  else if (r.tc)
+    e = launch_prefill_tc(a, r.qd, grid_tiles, st);
+  else
+    return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
+  if (e != cudaSuccess || grid_tiles == 0) return e;
+  return launch_pf_merge(a, r.qd, r.pf_bm, mixed, st);
 }
 
 }  // namespace
@@ -286,7 +325,7 @@ extern "C" {
 size_t paged_attn_workspace_size(const pa_params* params, int32_t num_rows, int32_t total_q) {
   Resolved r;
   if (resolve_params(params, &r) != PA_OK || num_rows < 0 || total_q < 0) return 0;
-  return workspace_layout(num_rows, total_q, r.hq, r.d, r.max_dq, r.g).total;
+  return workspace_layout(num_rows, total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts).total;
 }
 
 pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, const void* q,
@@ -300,11 +339,12 @@ pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, con
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
   const int bm = r.pf_bm;
-  const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
+  const int max_tiles =
+      (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm, r.pf_cut);
   cudaError_t e = launch_plan(a, 0, 0, bm, max_tiles, st);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   const int grid = r.host ? r.host_tiles : max_tiles;
-  return cuda_status(run_prefill(a, r, grid, st));
+  return cuda_status(run_prefill(a, r, grid, 0, st));
 }
 
 pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, const void* q,
@@ -333,13 +373,15 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   if (batch->num_rows == 0 || batch->total_q == 0) return PA_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
-  const WsLayout w = workspace_layout(batch->num_rows, batch->total_q, r.hq, r.d, r.max_dq, r.g);
+  const WsLayout w = workspace_layout(batch->num_rows, batch->total_q, r.hq, r.d, r.max_dq, r.g,
+                                     r.pf_parts);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   a.dec_base = reinterpret_cast<const int32_t*>(base + w.dec_base);
   a.slot_tok = reinterpret_cast<const int32_t*>(base + w.slot_tok);
   a.n_slots = &reinterpret_cast<const WsHeader*>(base)->n_slots;
   const int bm = r.pf_bm;
-  const int max_tiles = (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm);
+  const int max_tiles =
+      (int)max_tiles_for(batch->num_rows, batch->total_q, r.g, bm, r.pf_cut);
   cudaError_t e = launch_plan(a, 1, r.max_dq, bm, max_tiles, st);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   // decode rows: the grid covers every row; rows routed to prefill exit at once
@@ -364,7 +406,7 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (aux && cudaEventRecord(aux->join, aux->st) != cudaSuccess) return PA_ERR_CUDA;
-  e = run_prefill(a, r, grid, st);
+  e = run_prefill(a, r, grid, 1, st);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (aux && cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;

@@ -58,7 +58,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
     }
     if (qs < 0 || qs + qb > p.total_q) qb = 0;  // malformed row: the kernels skip it too
     const bool dec = mixed && qb >= 1 && qb <= max_dq;
-    const int nt = (!dec && qb > 0) ? (qb * p.g + bm - 1) / bm : 0;
+    const int nmb = (!dec && qb > 0) ? (qb * p.g + bm - 1) / bm : 0;
+    // work items of the row: one per m-block, or one per key-range part
+    int nt = nmb;
+    if (a.pf_parts > 1 && nmb > 0) {
+      const int L = p.seq_lens[b];
+      nt = 0;
+      for (int m = 0; m < nmb; ++m) {
+        int per;
+        const int r_last = min((m + 1) * bm, qb * p.g) - 1;
+        nt += max(1, pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per));
+      }
+    }
     const int ns = dec ? qb : 0;
     s_tiles[tid] = nt;
     s_slots[tid] = ns;
@@ -78,8 +89,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
       if (mixed) dec_base[b] = dec ? s_off : -1;
       for (int k = 0; k < ns; ++k)
         if (s_off + k < max_slots) slot_tok[s_off + k] = qs + k;
-      for (int m = 0; m < nt; ++m)
-        if (t_off + m < max_tiles) tiles[t_off + m] = make_int2(b, nt - 1 - m);
+      if (nt == nmb) {
+        for (int m = 0; m < nt; ++m)
+          if (t_off + m < max_tiles) tiles[t_off + m] = make_int2(b, nt - 1 - m);
+      } else {
+        const int L = p.seq_lens[b];
+        int k = t_off;
+        for (int m = nmb - 1; m >= 0; --m) {
+          int per;
+          const int r_last = min((m + 1) * bm, qb * p.g) - 1;
+          const int parts =
+              max(1, pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per));
+          for (int c = 0; c < parts; ++c, ++k)
+            if (k < max_tiles) tiles[k] = make_int2(b, m | (c << 24));
+        }
+      }
     }
     __syncthreads();
     if (tid == 1023) {
@@ -94,9 +118,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
   }
 
   // Longest-first order of the prefill work items (by the keys the item's
-  // rows can see), so the CTAs dispatched last are the short ones.  Items
-  // are independent, so the order changes no result.  Lists longer than
-  // 4096 items keep row order.
+  // rows can see, in its part), so the CTAs dispatched last are the short
+  // ones; equal items keep the parts of one key range together.  Items are
+  // independent, so the order changes no result.  Lists longer than 4096
+  // items keep row order.
   __syncthreads();
   const int n = min(s_tot_tiles, max_tiles);
   if (n < 2 || n > 4096) return;
@@ -110,11 +135,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
     unsigned long long key = 0ull;
     if (i < n) {
       const int2 t = tiles[i];
+      const int mb = t.y & 0xFFFFFF, c = t.y >> 24;
       const int qs = p.cu_q[t.x], qb = p.cu_q[t.x + 1] - qs, L = p.seq_lens[t.x];
-      const int r_last = min((t.y + 1) * bm, qb * p.g) - 1;
-      const int work = max(0, min(L, L - qb + r_last / p.g + 1));
-      if (t.x >= (1 << 20) || t.y >= (1 << 12)) s_bad = 1;
-      key = ((unsigned long long)(unsigned)work << 32) | ((unsigned)t.x << 12) | (unsigned)t.y;
+      const int r_last = min((mb + 1) * bm, qb * p.g) - 1;
+      int work = max(0, min(L, L - qb + r_last / p.g + 1));
+      if (a.pf_parts > 1) {
+        int per;
+        if (pf_part_count(work, a.pf_parts, &per) > 1)
+          work = min(work - c * per * PF_UNIT, per * PF_UNIT);
+      }
+      if (t.x >= (1 << 20) || mb >= (1 << 14) || c >= 16) s_bad = 1;
+      // 26 bits of work (64-key units), row, part, m-block
+      const unsigned long long w64 = (unsigned long long)((unsigned)work + 63u) >> 6;
+      key = (w64 << 38) | ((unsigned long long)t.x << 18) | ((unsigned)c << 14) | (unsigned)mb;
     }
     keys[i] = key;
   }
@@ -123,7 +156,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
   bitonic_sort_desc(keys, npow);
   for (int i = tid; i < n; i += 1024) {
     const unsigned long long key = keys[i];
-    tiles[i] = make_int2((int)((key >> 12) & 0xFFFFFu), (int)(key & 0xFFFu));
+    const int c = (int)((key >> 14) & 0xFu), mb = (int)(key & 0x3FFFu);
+    tiles[i] = make_int2((int)((key >> 18) & 0xFFFFFu), mb | (c << 24));
   }
 }
 
@@ -258,6 +292,84 @@ cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream
     PA_M(__half, 64) PA_M(__half, 128) PA_M(__half, 256)
   } else if (q_dtype == PA_F32) {
     PA_M(float, 64) PA_M(float, 128) PA_M(float, 256)
+  }
+#undef PA_M
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Merge of prefill key-range parts (1Cat-vLLM PR #1279, commit 5: the parts
+// of a CTA's key range combined by log-sum-exp).  For one prefill token and
+// query head whose work item was cut: M = max_c m_c over the parts with
+// l_c > 0, w_c = 2^(m_c - M), out = (sum_c w_c acc_c) / (sum_c w_c l_c) *
+// v_scale in the fixed order c = 0, 1, ...  The part count is recomputed
+// from the work item's key count exactly as the plan kernel cut it.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(64) pf_merge_kernel(const AttnArgs a, int bm, int mixed) {
+  const Problem& p = a.p;
+  const int t = blockIdx.x, h = blockIdx.y;
+  int lo = 0, hi = p.num_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int qs = __ldg(p.cu_q + b), qb = __ldg(p.cu_q + b + 1) - qs;
+  if (t < qs || t >= qs + qb || qs + qb > p.total_q) return;
+  if (mixed && qb <= a.max_decode_q) return;  // a decode row
+  const int L = __ldg(p.seq_lens + b);
+  const int M = qb * p.g;
+  const int R = (t - qs) * p.g + h % p.g;  // GQA-packed row within the row's query rows
+  const int mb = R / bm;
+  const int r_last = min((mb + 1) * bm, M) - 1;
+  int per;
+  const int parts = pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per);
+  if (parts <= 1) return;  // written by the prefill kernel itself
+
+  const float2* ml = a.pf_ml + ((int64_t)t * p.hq + h) * a.pf_parts;
+  float mstar = -INFINITY;
+  for (int c = 0; c < parts; ++c) {
+    const float2 v = ml[c];
+    if (v.y > 0.f) mstar = fmaxf(mstar, v.x);
+  }
+  float w[PF_MAX_PARTS];
+  float lsum = 0.f;
+#pragma unroll
+  for (int c = 0; c < PF_MAX_PARTS; ++c) {
+    w[c] = 0.f;
+    if (c < parts) {
+      const float2 v = ml[c];
+      if (v.y > 0.f) {
+        w[c] = exp2f(v.x - mstar);
+        lsum += w[c] * v.y;
+      }
+    }
+  }
+  const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+  const float* acc = a.pf_acc + ((int64_t)t * p.hq + h) * a.pf_parts * D;
+  T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
+  for (int col = threadIdx.x; col < D; col += 64) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < PF_MAX_PARTS; ++c)
+      if (w[c] != 0.f) s += w[c] * acc[c * D + col];
+    out[col] = from_float<T>(s * inv);
+  }
+}
+
+cudaError_t launch_pf_merge(const AttnArgs& a, int q_dtype, int bm, int mixed, cudaStream_t st) {
+  if (a.pf_parts <= 1 || a.p.total_q == 0 || a.p.num_rows == 0) return cudaSuccess;
+  dim3 grid(a.p.total_q, a.p.hq);
+#define PA_M(TT, DD)                                                   \
+  if (a.p.d == DD) {                                                   \
+    pf_merge_kernel<TT, DD><<<grid, 64, 0, st>>>(a, bm, mixed);        \
+    return cudaGetLastError();                                         \
+  }
+  if (q_dtype == PA_BF16) {
+    PA_M(__nv_bfloat16, 64) PA_M(__nv_bfloat16, 128) PA_M(__nv_bfloat16, 256)
+  } else if (q_dtype == PA_F16) {
+    PA_M(__half, 64) PA_M(__half, 128) PA_M(__half, 256)
   }
 #undef PA_M
   return cudaErrorInvalidValue;

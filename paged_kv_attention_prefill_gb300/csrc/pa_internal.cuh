@@ -47,6 +47,8 @@ struct WsLayout {
   size_t tiles;      // int2  [max_tiles]  (row, m-block) prefill work items
   size_t part_acc;   // float [max_slots, Hq, NSPLIT, d]
   size_t part_ml;    // float2[max_slots, Hq, NSPLIT]  (m in log2 units, l)
+  size_t pf_ml;      // float2[total_q, Hq, pf_parts]  prefill key-range parts (0 bytes when off)
+  size_t pf_acc;     // float [total_q, Hq, pf_parts, d]
   size_t total;
   int64_t max_slots;
   int64_t max_tiles;
@@ -57,7 +59,36 @@ constexpr int DEC_KT = 64;      // keys per decode tile; the split partition uni
 constexpr int DEC_ROWS = 16;    // GQA-packed query rows per decode CTA
 constexpr int PF_BM = 64;       // GQA-packed query rows per prefill CTA (mma.sync path)
 
-WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g);
+// Prefill key-range parts (1Cat-vLLM PR #1279, commit 5: a CTA's key range
+// cut into whole-tile ranges merged by log-sum-exp).  A work item's keys
+// [0, k_end) are counted in units of PF_UNIT keys (a multiple of every
+// prefill key tile) and cut into at most `max_parts` parts of equal whole
+// units, one part per PF_PART_UNITS units or fewer: the cut depends on k_end
+// alone, so a row's result never depends on the rest of the batch, the page
+// size or the physical pages.
+constexpr int PF_UNIT = 128;
+constexpr int PF_PART_UNITS = 128;   // 16384 keys
+constexpr int PF_MAX_PARTS = 16;
+
+WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g,
+                          int pf_parts);
+
+// Parts of a work item whose rows see keys [0, k_end): sets the units per
+// part (the last part takes the remainder) and returns the part count (0 for
+// k_end <= 0, 1 when not cut).
+__host__ __device__ inline int pf_part_count(int k_end, int max_parts, int* per_units) {
+  if (k_end <= 0) {
+    *per_units = 0;
+    return 0;
+  }
+  const int n_u = (k_end + PF_UNIT - 1) / PF_UNIT;
+  int parts = max_parts > 1 ? (n_u + PF_PART_UNITS - 1) / PF_PART_UNITS : 1;
+  if (parts > max_parts) parts = max_parts;
+  if (parts < 1) parts = 1;
+  const int per = (n_u + parts - 1) / parts;
+  *per_units = per;
+  return (n_u + per - 1) / per;
+}
 
 // ---------------------------------------------------------------------------
 // Device-side problem description, passed by value to every kernel.
@@ -88,8 +119,11 @@ struct AttnArgs {
   const int32_t* dec_base;   // mixed: slot base per row (-1: not a decode row); null: slot = token
   const int32_t* slot_tok;   // mixed: global token per slot; null: slot = token
   const int32_t* row_order;  // decode work order of the rows; null: row order
-  const int2* tiles;         // prefill work list
+  const int2* tiles;         // prefill work list: (row, m-block | part << 24)
   const uint32_t* n_tiles;   // its length (device)
+  int pf_parts;              // prefill key-range parts per work item at most (<= 1: not cut)
+  float* pf_acc;             // partial states of cut work items
+  float2* pf_ml;
   int max_decode_q;
   int64_t max_slots;         // decode slots the workspace holds
   int dec_mblk;              // decode grid: 16-row query blocks per row (per token if tokenwise)
@@ -105,6 +139,9 @@ cudaError_t launch_decode_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int 
 cudaError_t launch_prefill_mma(const AttnArgs& a, int q_dtype, int kv_dtype, int max_tiles,
                                cudaStream_t st);
 cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream_t st);
+// Merges the key-range parts of the prefill work items that were cut (bm:
+// query rows per work item); tokens of uncut items are left as written.
+cudaError_t launch_pf_merge(const AttnArgs& a, int q_dtype, int bm, int mixed, cudaStream_t st);
 // Rows with more work per decode split first (rows off the decode path
 // last); written to `order` for 2 <= num_rows <= MAX_ORDER_ROWS.
 constexpr int MAX_ORDER_ROWS = 4096;

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(384, 1)
   const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
   if (item >= (int)*a.n_tiles) return;
   const int2 wi = a.tiles[item];
-  const int b = wi.x, mb = wi.y;
+  const int b = wi.x, mb = wi.y & 0xFFFFFF, part = wi.y >> 24;
   const int qs = __ldg(p.cu_q + b);
   const int qb = __ldg(p.cu_q + b + 1) - qs;
   const int L = __ldg(p.seq_lens + b);
@@ -162,7 +162,12 @@ __global__ void __launch_bounds__(384, 1)
   if (R0 >= M) return;
   const int r_last = min(R0 + C::BM, M) - 1;
   const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
-  const int n_tiles = k_end > 0 ? (k_end + C::BN - 1) / C::BN : 0;
+  // the item's key range [k0, k1): the whole range, or one part of it
+  int per_u;
+  const bool cut = pf_part_count(k_end, a.pf_parts, &per_u) > 1;
+  const int k0 = cut ? part * per_u * PF_UNIT : 0;
+  const int k1 = cut ? min(k_end, (part + 1) * per_u * PF_UNIT) : k_end;
+  const int n_tiles = k1 > k0 ? (k1 - k0 + C::BN - 1) / C::BN : 0;
 
   // ---- barriers and TMEM ----------------------------------------------------
   if (threadIdx.x == 0) {
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
-      const int kbase = j * C::BN;
+      const int kbase = k0 + j * C::BN;
       const uint32_t dst = ring + st * C::KV_BYTES;
       // slot `lane`: 1 = whole slot by TMA, 2 = partial (copied by hand), 3 = zero-fill
       int kind = 0, tok0 = 0;
@@ -365,7 +370,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_SE + buf));
 
-      const int kb = j * C::BN + hf * HN;
+      const int kb = k0 + j * C::BN + hf * HN;
       if (kb + HN - 1 > last) {
 #pragma unroll
         for (int k = 0; k < HN; ++k)
@@ -451,7 +456,27 @@ __global__ void __launch_bounds__(384, 1)
       lt = hf == 0 ? l + lo : lo + l;  // the same sum in both warpgroups
     }
     T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
-    if (n_tiles > 0) {
+    if (cut) {
+      // this part's unnormalised O (each warpgroup its d / 2 columns), the
+      // maximum it is relative to and the row sum, for the merge
+      const int64_t slot = ((int64_t)(qs + i) * p.hq + kh * g + hg) * a.pf_parts + part;
+      if (valid && hf == 0)
+        a.pf_ml[slot] = make_float2(n_tiles > 0 ? m_used : -INFINITY, n_tiles > 0 ? lt : 0.f);
+      float* prow = a.pf_acc + slot * D + hf * HD;
+      if (n_tiles > 0) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              *reinterpret_cast<uint4*>(prow + c * 32 + 4 * w) =
+                  make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+          }
+        }
+      }
+    } else if (n_tiles > 0) {
       const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {

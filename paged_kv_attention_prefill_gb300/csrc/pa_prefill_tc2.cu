@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t bar0 = base + C::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
+  // the item's part index when its key range is cut, else -1 (read back by
+  // the epilogue, so the softmax warps need not keep it in registers)
+  volatile int* part_slot = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 248);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   const Problem& p = a.p;
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(384, 1)
   const int item = blockIdx.x / p.hkv, kh = blockIdx.x % p.hkv;
   if (item >= (int)*a.n_tiles) return;
   const int2 wi = a.tiles[item];
-  const int b = wi.x, mb = wi.y;
+  const int b = wi.x, mb = wi.y & 0xFFFFFF, part = wi.y >> 24;
   const int qs = __ldg(p.cu_q + b);
   const int qb = __ldg(p.cu_q + b + 1) - qs;
   const int L = __ldg(p.seq_lens + b);
@@ -157,12 +160,22 @@ __global__ void __launch_bounds__(384, 1)
   }
   const int g = p.g, M = qb * g, R0 = mb * 2 * C::BM;
   if (R0 >= M) return;
-  // key tiles of each query tile (0 for an empty tile B)
+  // keys any row of a query tile (of the item) sees
+  auto k_end_of = [&](int r0, int rows) {
+    const int r_last = min(r0 + rows, M) - 1;
+    return min(L, L - qb + r_last / g + 1);
+  };
+  // The item's key range [k0, k1): the whole range, or one part of it
+  int per_u;
+  const int k_item = k_end_of(R0, 2 * C::BM);
+  const bool cut = pf_part_count(k_item, a.pf_parts, &per_u) > 1;
+  const int k0 = cut ? part * per_u * PF_UNIT : 0;
+  const int k1 = cut ? min(k_item, (part + 1) * per_u * PF_UNIT) : k_item;
+  // key tiles of each query tile in the range (0 for an empty tile B)
   auto tiles_of = [&](int r0) {
     if (r0 >= M) return 0;
-    const int r_last = min(r0 + C::BM, M) - 1;
-    const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile sees
-    return k_end > 0 ? (k_end + C::BN - 1) / C::BN : 0;
+    const int hi = min(k_end_of(r0, C::BM), k1);
+    return hi > k0 ? (hi - k0 + C::BN - 1) / C::BN : 0;
   };
   const int nA = tiles_of(R0), nB = tiles_of(R0 + C::BM);
   const int n_kv = max(nA, nB);
@@ -192,6 +205,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_V8E + s), 2);
     }
     *abort_flag = 0;
+    *part_slot = cut ? part : -1;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -221,7 +235,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       for (; j < n_kv; ++j) {
         const int st = j % C::S8;
-        const int kbase = j * C::BN;
+        const int kbase = k0 + j * C::BN;
         int kind = 0, tok0 = 0;
         if (lane < C::SLOTS) {
           const int s0 = kbase + 16 * lane;
@@ -354,7 +368,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        const int kbase = j * C::BN;
+        const int kbase = k0 + j * C::BN;
         const uint32_t dst = ring + st * C::KV_BYTES;
         // slot `lane`: 1 = whole slot by TMA, 2 = partial (copied by hand), 3 = zero-fill
         int kind = 0, tok0 = 0;
@@ -501,7 +515,8 @@ __global__ void __launch_bounds__(384, 1)
     const int R = R0 + t * C::BM + r;
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
-    const int last = valid ? L - qb + i : -1;  // last visible key of this row
+    // last visible key of this row, counted from the start of the key range
+    const int last = valid ? L - qb + i - k0 : -1 - k0;
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
     const int n = t ? nB : nA;
     const uint32_t q_t = sQ + t * C::Q_BYTES;
@@ -592,9 +607,33 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_PF + t));
     }
-    // ---- epilogue: out = O / l * v_scale ----
+    // ---- epilogue: out = O / l * v_scale, or this part's (O, m, l) ----
     T* orow = static_cast<T*>(a.out) + qoff;
-    if (n > 0) {
+    const int part_e = *part_slot;
+    if (part_e >= 0) {
+      // unnormalised O, the maximum it is relative to and the row sum, for
+      // the merge (a row that saw no key of the part: l = 0, skipped there)
+      const int64_t slot = ((int64_t)(qs + i) * p.hq + kh * g + hg) * a.pf_parts + part_e;
+      if (n > 0) {
+        mbar_wait(bar(C::B_OF + t), (n - 1) & 1, abort_flag, p.err);
+        tc_fence_after();
+      }
+      if (valid) a.pf_ml[slot] = make_float2(n > 0 ? m_used : -INFINITY, n > 0 ? l : 0.f);
+      float* prow = a.pf_acc + slot * D;
+      if (n > 0) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::BN + c * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              *reinterpret_cast<uint4*>(prow + c * 32 + 4 * w) =
+                  make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+          }
+        }
+      }
+    } else if (n > 0) {
       mbar_wait(bar(C::B_OF + t), (n - 1) & 1, abort_flag, p.err);
       tc_fence_after();
       const float inv = l > 0.f ? p.v_scale / l : 0.f;

@@ -136,7 +136,7 @@ def test_rejects_bad_batches(lib, name):
     assert c(name, k=None) == INVALID                                   # null cache
     small = FakeCall(lib, p, [1, 1], [10, 20], ws_bytes=1024)
     assert small(name) == WS_SMALL
-    assert lib.__getattr__(name)(None, None, None, None, None, None, None, 0, None) == INVALID
+    assert getattr(lib, name)(None, None, None, None, None, None, None, 0, None) == INVALID
 
 
 def test_decode_rejects_long_rows_with_host_mirrors(lib):
@@ -160,6 +160,26 @@ def test_valid_call_without_gpu_stops_at_device_check(lib, name):
 def test_empty_batch_is_ok_or_no_device(lib):
     for name in ENTRIES:
         assert FakeCall(lib, params(), [], [])(name) in (OK, NO_DEVICE)
+
+
+def test_prefill_parts_workspace_and_checks(lib):
+    # K prefill parts add K fp32 states (acc[d], m, l) per query token and head
+    # (and K times the work-list entries); 0 and 1 leave the workspace as it is
+    base = pa.workspace_size(params(), 8, 1000)
+    assert pa.workspace_size(params(prefill_kv_parts=1), 8, 1000) == base
+    for k in (2, 8, 16):
+        grown = pa.workspace_size(params(prefill_kv_parts=k), 8, 1000) - base
+        states = 1000 * 16 * k * (128 + 2) * 4
+        assert states <= grown <= states + 1000 * 16 * k * 8 + 64 * 1024
+    for bad in (-1, 17):
+        assert lib.paged_attn_workspace_size(ctypes.byref(params(prefill_kv_parts=bad)), 4, 4) == 0
+        for name in ENTRIES:
+            assert FakeCall(lib, params(prefill_kv_parts=bad), [1, 1], [10, 20])(name) == INVALID
+    # decode never cuts prefill items: its workspace need is the uncut one
+    p = params(prefill_kv_parts=8)
+    c = FakeCall(lib, p, [1, 1], [10, 20], ws_bytes=pa.workspace_size(params(), 2, 2))
+    assert c("paged_attn_decode") in (OK, NO_DEVICE)
+    assert c("paged_attn_prefill") == WS_SMALL
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
