@@ -45,9 +45,14 @@ using namespace sm100;
 
 // Registers per thread at launch (384 threads, one CTA per SM) and after the
 // split, which must fit in what the CTA was launched with:
-// 128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH.
-constexpr int REG_LAUNCH = 168, REG_LOW = 72, REG_HIGH = 216;
-static_assert(128 * REG_LOW + 256 * REG_HIGH <= 384 * REG_LAUNCH, "register split");
+// 128 * reg_low + 256 * reg_high <= 384 * REG_LAUNCH.  With an fp8 cache the
+// producer / widening warpgroup needs more.
+constexpr int REG_LAUNCH = 168;
+constexpr int reg_low(bool kv8) { return kv8 ? 88 : 72; }
+constexpr int reg_high(bool kv8) { return kv8 ? 200 : 216; }
+static_assert(128 * reg_low(false) + 256 * reg_high(false) <= 384 * REG_LAUNCH &&
+                  128 * reg_low(true) + 256 * reg_high(true) <= 384 * REG_LAUNCH,
+              "register split");
 
 template <int D, bool KV8>
 struct Tc2Cfg {
@@ -71,7 +76,8 @@ struct Tc2Cfg {
   static constexpr uint32_t OFF_K8 = OFF_V + VS * KV_BYTES;
   static constexpr uint32_t OFF_V8 = OFF_K8 + (KV8 ? S8 * KV8_BYTES : 0);
   static constexpr uint32_t OFF_BAR = OFF_V8 + (KV8 ? S8 * KV8_BYTES : 0);
-  static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
+  static constexpr uint32_t BAR_AREA = 320;        // mbarriers, then TMEM address and flags
+  static constexpr uint32_t SMEM = OFF_BAR + BAR_AREA + 16 + 1024;  // alignment slack
   // TMEM: tile t owns columns [t * TILE_COLS, +BN) for S (P over it) and
   // [t * TILE_COLS + BN, +D) for O.
   static constexpr uint32_t TILE_COLS = BN + D;
@@ -79,15 +85,16 @@ struct Tc2Cfg {
   // barrier indices
   static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
                        B_SF = 2 * KS + 2 * VS,  // [2] S_t written
-      B_PF = B_SF + 2,                          // [2] P_t written (128 arrivals)
-      B_OF = B_PF + 2,                          // [2] O_t += P_t V done
+      B_PF = B_SF + 2,                          // [2] P_t of keys 0-63 written (128 arrivals)
+      B_PF2 = B_PF + 2,                         // [2] P_t of keys 64-127 written (128 arrivals)
+      B_OF = B_PF2 + 2,                         // [2] O_t += P_t V done
       B_Q = B_OF + 2,                           // [2] Q_t staged (128 arrivals)
       B_DRAIN = B_Q + 2,                        // every MMA done
       B_K8F = B_DRAIN + 1, B_K8E = B_K8F + S8,  // fp8 code rings: full / empty
       B_V8F = B_K8E + S8, B_V8E = B_V8F + S8, NBAR = B_V8E + S8;
   static_assert(2 * TILE_COLS <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NBAR * 8 <= 240, "barrier area");
+  static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
   static_assert(!KV8 || D == 128, "fp8 caches: one 128-byte TMA box per key row");
 };
 
@@ -133,11 +140,11 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
   const uint32_t sK8 = base + C::OFF_K8, sV8 = base + C::OFF_V8;
   const uint32_t bar0 = base + C::OFF_BAR;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 240);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::BAR_AREA);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::BAR_AREA + 4);
   // the item's part index when its key range is cut, else -1 (read back by
   // the epilogue, so the softmax warps need not keep it in registers)
-  volatile int* part_slot = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 248);
+  volatile int* part_slot = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::BAR_AREA + 8);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   const Problem& p = a.p;
@@ -194,6 +201,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SF + t), 1);
       mbar_init(bar(C::B_PF + t), 128);
+      mbar_init(bar(C::B_PF2 + t), 128);
       mbar_init(bar(C::B_OF + t), 1);
       mbar_init(bar(C::B_Q + t), 128);
     }
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    setmaxnreg_dec<REG_LOW>();
+    setmaxnreg_dec<reg_low(KV8)>();
     if (KV8 && warp == 0) {
       // ===== fp8 cache: warp 0 streams the K and V codes of each key tile ======
       // into the code rings, one TMA box (16 keys x 128 codes) per page slot;
@@ -442,30 +450,39 @@ __global__ void __launch_bounds__(384, 1)
           const int st = j % C::KS;
           if (!mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err)) return false;
           tc_fence_after();
-          const uint32_t q_t = sQ + t * C::Q_BYTES;
+          // descriptors of the first step; later steps add their byte offset
+          // (>> 4) to the start-address field, which never carries out of it.
+          // The issue cost is on the critical path: one MMA is 64 cycles of
+          // tensor work.
+          const uint64_t a0 = sdesc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+          const uint64_t b0 = sdesc_sw128(sK + st * C::KV_BYTES, 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint64_t ad =
-                sdesc_sw128(q_t + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(
-                sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t ad = a0 + (uint64_t)(((k >> 2) * (C::BM * 128) + (k & 3) * 32) >> 4);
+            const uint64_t bd = b0 + (uint64_t)(((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4);
             tc_mma_f16(tmem + t * C::TILE_COLS, ad, bd, idS, k > 0 ? 1u : 0u);
           }
           tc_commit(bar(C::B_SF + t));
           return true;
         };
         auto issue_PV = [&](int t, int j) {
+          // in two halves of 64 keys: the first half's products start while
+          // the softmax still computes the second half's P
           const int sv = j % C::VS;
-          if (!mbar_wait(bar(C::B_PF + t), j & 1, abort_flag, p.err) ||
-              !mbar_wait(bar(C::B_VF + sv), (j / C::VS) & 1, abort_flag, p.err))
-            return false;
-          tc_fence_after();
+          if (!mbar_wait(bar(C::B_VF + sv), (j / C::VS) & 1, abort_flag, p.err)) return false;
           const uint32_t tb = tmem + t * C::TILE_COLS;
+          const uint64_t b0 = sdesc_sw128(sV + sv * C::KV_BYTES, C::BN * 128, 1024);
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k) {
-            // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
-            const uint64_t bd = sdesc_sw128(sV + sv * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-            tc_mma_f16_ts(tb + C::BN, tb + 8 * k, bd, idO, (j > 0 || k > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(bar((h ? C::B_PF2 : C::B_PF) + t), j & 1, abort_flag, p.err))
+              return false;
+            tc_fence_after();
+#pragma unroll
+            for (int k = h * C::BN / 32; k < (h + 1) * C::BN / 32; ++k) {
+              // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
+              const uint64_t bd = b0 + (uint64_t)((k * 16 * 128) >> 4);
+              tc_mma_f16_ts(tb + C::BN, tb + 8 * k, bd, idO, (j > 0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(bar(C::B_OF + t));
           return true;
@@ -504,7 +521,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
     }
   } else {
-    setmaxnreg_inc<REG_HIGH>();
+    setmaxnreg_inc<reg_high(KV8)>();
     // ============ softmax and epilogue of query tile t ========================
     // Thread = one query row = one TMEM lane of the tile.  The loop never
     // leaves early: after a timed-out wait it runs on (flag raised, waits
@@ -575,13 +592,8 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_new;
       }
       const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
-#pragma unroll
-      for (int k = 0; k < C::BN; ++k) {
-        x[k] = ex2(fmaf(x[k], sl2, nmu));
-        ps[k & 7] += x[k];
-      }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      // O is rescaled before any of this tile's P is published (the P V
+      // product of the previous tile is done: S_t(j) was issued after it)
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -592,20 +604,26 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st_x32(trow + C::BN + c * 32, o);
         }
       }
-      l = l * factor + rs;
-      {
-        // P (16-bit pairs) over the first BN / 2 columns of S
+      // P (16-bit pairs) over the first BN / 2 columns of S, in two halves of
+      // 64 keys, each published as soon as it is in TMEM
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int k = 64 * h; k < 64 * h + 64; ++k) {
+          x[k] = ex2(fmaf(x[k], sl2, nmu));
+          ps[k & 7] += x[k];
+        }
         uint32_t pk[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) pk[k] = pack2<T>(x[64 * h + 2 * k], x[64 * h + 2 * k + 1]);
-          tmem_st_x32_nowait(trow + 32 * h, pk);
-        }
+        for (int k = 0; k < 32; ++k) pk[k] = pack2<T>(x[64 * h + 2 * k], x[64 * h + 2 * k + 1]);
+        tmem_st_x32_nowait(trow + 32 * h, pk);
         tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar((h ? C::B_PF2 : C::B_PF) + t));
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PF + t));
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l = l * factor + rs;
     }
     // ---- epilogue: out = O / l * v_scale, or this part's (O, m, l) ----
     T* orow = static_cast<T*>(a.out) + qoff;
