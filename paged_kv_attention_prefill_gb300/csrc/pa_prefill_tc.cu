@@ -292,11 +292,15 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t dS = tmem + buf * C::BN;
+          // descriptors of the first step; later steps add their byte offset
+          // (>> 4) to the start-address field, which never carries out of it
+          // (the issue cost of these short MMAs is on the critical path)
+          const uint64_t a0 = sdesc_sw128(sQ, 16, 1024);
+          const uint64_t b0 = sdesc_sw128(sK + st * C::KV_BYTES, 16, 1024);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(sQ + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(
-                sK + st * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t ad = a0 + (uint64_t)(((k >> 2) * (C::BM * 128) + (k & 3) * 32) >> 4);
+            const uint64_t bd = b0 + (uint64_t)(((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4);
             tc_mma_f16(dS, ad, bd, idS, k > 0 ? 1u : 0u);
           }
           tc_commit(bar(C::B_SF + buf));
@@ -308,11 +312,11 @@ __global__ void __launch_bounds__(384, 1)
           if (ok) ok = mbar_wait(bar(C::B_PF), jj & 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
+          const uint64_t v0 = sdesc_sw128(sV + stp * C::KV_BYTES, C::BN * 128, 1024);
 #pragma unroll
           for (int k = 0; k < C::BN / 16; ++k) {
             // A = P straight from TMEM: 16 keys = 8 columns of 16-bit pairs
-            const uint64_t bd =
-                sdesc_sw128(sV + stp * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
+            const uint64_t bd = v0 + (uint64_t)((k * 16 * 128) >> 4);
             tc_mma_f16_ts(tmem + C::O_COL, tmem + C::P_COL + 8 * k, bd, idO,
                           (jj > 0 || k > 0) ? 1u : 0u);
           }
