@@ -50,10 +50,10 @@ L2_BYTES = 129 * 1024 * 1024
 # Reported only while the kernel's sources are the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "9a0a4840221133f584833e6de02e98c05e199363e7a33a7901bec63d25ce79de",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "ca6e0fd53d0588174a82325b24677de60d0f5c76c47f14497ba392b24e84b523",
         "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "b118652fb223ae088defcdb22930b457bfd73b3d16884163b65a6288e74fcdb2",
     },
-    "bytes_per_launch": 956704000 + 55211008,
+    "bytes_per_launch": 957533184 + 54020352,
 }
 
 
