@@ -85,8 +85,8 @@ struct Tc2Cfg {
   // barrier indices
   static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
                        B_SF = 2 * KS + 2 * VS,  // [2] S_t written
-      B_PF = B_SF + 2,                          // [2] P_t of keys 0-63 written (128 arrivals)
-      B_PF2 = B_PF + 2,                         // [2] P_t of keys 64-127 written (128 arrivals)
+      B_PF = B_SF + 2,                          // [2] P_t of keys 0-63 written (4 warps)
+      B_PF2 = B_PF + 2,                         // [2] P_t of keys 64-127 written (4 warps)
       B_OF = B_PF2 + 2,                         // [2] O_t += P_t V done
       B_Q = B_OF + 2,                           // [2] Q_t staged (128 arrivals)
       B_DRAIN = B_Q + 2,                        // every MMA done
@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::B_SF + t), 1);
-      mbar_init(bar(C::B_PF + t), 128);
-      mbar_init(bar(C::B_PF2 + t), 128);
+      mbar_init(bar(C::B_PF + t), 4);
+      mbar_init(bar(C::B_PF2 + t), 4);
       mbar_init(bar(C::B_OF + t), 1);
       mbar_init(bar(C::B_Q + t), 128);
     }
@@ -620,7 +620,9 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st_x32_nowait(trow + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar((h ? C::B_PF2 : C::B_PF) + t));
+        // every lane's stores are done: one arrival per warp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar((h ? C::B_PF2 : C::B_PF) + t));
       }
       const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * factor + rs;
