@@ -272,6 +272,23 @@ def part_mixed3(steps, warmup, stream, pk):
             gbs = byt / (sms * 1e-3) / 1e9
             res[name] = {"ms": round(sms, 4), "GB/s": round(gbs, 1),
                          "frac_of_hbm": round(gbs / pk["hbm"], 4)}
+        if name.startswith("prefill"):
+            # the same row with the part count chosen per call (cut in 3 here)
+            aws = pa.make_workspace(pa.make_params(sb.q, sb.k_cache,
+                                                   prefill_kv_parts=pa.PA_PREFILL_PARTS_AUTO),
+                                    sb.num_rows, sb.total_q, "cuda")
+
+            def afn():
+                entry(sb.q, sb.k_cache, sb.v_cache, sb.block_table, sb.cu_seqlens_q, sb.seq_lens,
+                      out=sout, workspace=aws, prefill_kv_parts=pa.PA_PREFILL_PARTS_AUTO, **skw)
+            ams = time_calls(afn, steps, warmup, stream)
+            atf = F / (ams * 1e-3) / 1e12
+            res["prefill_row_alone_auto_parts"] = {
+                "ms": round(ams, 4), "TFLOP/s": round(atf, 1),
+                "frac_of_bf16_peak": round(atf / pk["bf16"], 4),
+                "note": "prefill_kv_parts = PA_PREFILL_PARTS_AUTO: key-range parts merged by "
+                        "log-sum-exp, count chosen for the device"}
+            del aws
         del sb, sws, sout
     del b, ws, out
     torch.cuda.empty_cache()

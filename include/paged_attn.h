@@ -62,8 +62,9 @@
  * stream).  They keep no state between calls except a per-device cache of
  * launch attributes, and are safe to call from several host threads with
  * distinct workspaces.  Results are deterministic: the same call gives the
- * same bits; a row's output does not depend on the other rows of the batch,
- * on the page size or on which physical pages hold it.
+ * same bits; a row's output does not depend on the other rows of the batch
+ * (prefill rows under PA_PREFILL_PARTS_AUTO excepted), on the page size or
+ * on which physical pages hold it.
  *
  * Every entry point returns a pa_status.  Host-detectable problems
  * (null pointers, bad sizes, unsupported types, a small workspace, and --
@@ -125,7 +126,8 @@ typedef struct pa_params {
                              PA_VERIFY_TOKENWISE (1), see below */
   int32_t prefill_kv_parts; /* prefill work items cut into key-range parts:
                                0 or 1 = not cut, 2..16 = at most this many
-                               parts, see below */
+                               parts, PA_PREFILL_PARTS_AUTO = chosen per
+                               call, see below */
 } pa_params;
 
 /*
@@ -162,8 +164,22 @@ enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
  * tcgen05 prefill (16-bit q with a same-type cache, or an E5M2 cache at
  * head_dim 128); other prefill paths ignore it.  The workspace grows by
  * total_q * Hq * K * (head_dim + 2) * 4 bytes; paged_attn_decode ignores the
- * field.  Values outside 0..16 return PA_ERR_INVALID_ARG.
+ * field.  Values outside 0..16 and PA_PREFILL_PARTS_AUTO return
+ * PA_ERR_INVALID_ARG.
+ *
+ * PA_PREFILL_PARTS_AUTO (-1): the part count (1 to 4) is chosen per call, the
+ * one whose work list -- items cut into equal runs of whole 128-key units,
+ * at least 1024 keys each, handed out longest first, one CTA per SM --
+ * finishes first on this device (1Cat-vLLM PR #1279, commit 5: the split
+ * count that takes the fewest full-CTA times); launches with four or more
+ * waves, or whose longest item has fewer than 8192 keys, are not cut.  It
+ * needs the host mirrors and applies only to calls without decode rows (a
+ * mixed call with decode rows, or any call without mirrors, is not cut).
+ * The count depends on the whole batch, so a prefill row's bits may differ
+ * between batches (still independent of the page size and the pages); the
+ * workspace is sized for 4 parts.
  */
+enum { PA_PREFILL_PARTS_AUTO = -1 };
 
 typedef struct pa_batch {
   int32_t num_rows;             /* B >= 0 */

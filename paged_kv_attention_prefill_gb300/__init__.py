@@ -54,6 +54,7 @@ class Params(ctypes.Structure):
                 ("prefill_kv_parts", ctypes.c_int32)]
 
 PA_VERIFY_PACKED, PA_VERIFY_TOKENWISE = 0, 1
+PA_PREFILL_PARTS_AUTO = -1
 
 
 class Batch(ctypes.Structure):

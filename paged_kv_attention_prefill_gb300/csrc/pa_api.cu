@@ -3,6 +3,9 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "pa_internal.cuh"
 
@@ -57,8 +60,10 @@ struct Resolved {
   bool tc;            // prefill on the tcgen05 kernel
   bool tc2;           // prefill on the two-tile tcgen05 kernel
   int pf_bm;          // query rows per prefill work item
-  int pf_parts;       // prefill_kv_parts as given (workspace layout)
+  int pf_parts;       // prefill parts the workspace holds (prefill_kv_parts, 4 for auto)
+  bool pf_auto;       // part count chosen per call
   int pf_cut;         // key-range parts in use (the tcgen05 kernels cut; others do not)
+  int pf_min_units;   // least 128-key units per part
 };
 
 // 0 = not checked, 1 = sm_103, 2 = other
@@ -111,13 +116,79 @@ pa_status resolve_params(const pa_params* prm, Resolved* r) {
   if (prm->verify_mode != PA_VERIFY_PACKED && prm->verify_mode != PA_VERIFY_TOKENWISE)
     return PA_ERR_INVALID_ARG;
   r->tokenwise = prm->verify_mode == PA_VERIFY_TOKENWISE;
-  if (prm->prefill_kv_parts < 0 || prm->prefill_kv_parts > PF_MAX_PARTS) return PA_ERR_INVALID_ARG;
-  r->pf_parts = prm->prefill_kv_parts;
+  r->pf_auto = prm->prefill_kv_parts == PA_PREFILL_PARTS_AUTO;
+  if (!r->pf_auto && (prm->prefill_kv_parts < 0 || prm->prefill_kv_parts > PF_MAX_PARTS))
+    return PA_ERR_INVALID_ARG;
+  r->pf_parts = r->pf_auto ? PF_AUTO_MAX : prm->prefill_kv_parts;
   r->pf_cut = 0;
+  r->pf_min_units = PF_PART_UNITS;
   return PA_OK;
 }
 
 enum Entry { E_PREFILL, E_DECODE, E_MIXED };
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Part count for prefill_kv_parts = PA_PREFILL_PARTS_AUTO (1Cat-vLLM PR #1279,
+// commit 5: the launcher picks the split count, up to 4, that finishes in the
+// fewest full-CTA times on the device).  The work items' key counts are known
+// from the host mirrors; for K = 1..4 the items are cut (equal runs of whole
+// 128-key units, at least PF_AUTO_UNITS each) and the CTAs (one per item,
+// part and KV head, one per SM) are handed out longest first to the earliest
+// free SM, the way the work list is ordered and the hardware dispatches it;
+// a CTA costs its 128-key units plus a fixed start-up.  The K with the
+// earliest finish wins; a cut must beat K = 1 by 3 % (its merge costs too).
+// Launches with four or more waves of CTAs, or with short items, are not cut.
+int choose_parts(const std::vector<int>& k_ends, int hkv, int sms) {
+  constexpr double START_UNITS = 2.0;
+  const int64_t n1 = (int64_t)k_ends.size() * hkv;
+  if (sms <= 0 || n1 == 0 || n1 >= 4LL * sms) return 1;
+  int longest = 0;
+  for (int k : k_ends) longest = std::max(longest, k);
+  if (longest < 64 * PF_UNIT) return 1;
+  double base = 0.0, best = 0.0;
+  int best_k = 1;
+  std::vector<double> cost;
+  for (int K = 1; K <= PF_AUTO_MAX; ++K) {
+    cost.clear();
+    for (int k : k_ends) {
+      int per = 0;
+      const int parts = std::max(1, pf_part_count(k, K, PF_AUTO_UNITS, &per));
+      const int n_u = (std::max(k, 0) + PF_UNIT - 1) / PF_UNIT;
+      for (int c = 0; c < parts; ++c) {
+        const int units = parts == 1 ? n_u : std::min(per, n_u - c * per);
+        for (int h = 0; h < hkv; ++h) cost.push_back(units + START_UNITS);
+      }
+    }
+    std::sort(cost.begin(), cost.end(), std::greater<double>());
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int s = 0; s < sms; ++s) free_at.push(0.0);
+    double finish = 0.0;
+    for (double c : cost) {
+      const double t = free_at.top() + c;
+      free_at.pop();
+      free_at.push(t);
+      finish = std::max(finish, t);
+    }
+    if (K == 1) {
+      base = best = finish;
+    } else if (finish < 0.97 * base && finish < best) {
+      best = finish;
+      best_k = K;
+    }
+  }
+  return best_k;
+}
 
 pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const void* q,
                    const void* kc, const void* vc, void* out, void* ws, size_t ws_bytes,
@@ -147,7 +218,9 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
     return PA_ERR_UNSUPPORTED;
   r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
-  r->pf_cut = (r->tc2 || r->tc) && r->pf_parts > 1 ? r->pf_parts : 0;
+  // an explicit part count applies as given; a count chosen per call needs
+  // the host mirrors (below)
+  r->pf_cut = (r->tc2 || r->tc) && !r->pf_auto && r->pf_parts > 1 ? r->pf_parts : 0;
   r->host = bat->cu_seqlens_q_host && bat->seq_lens_host;
   r->host_max_q_dec = 0;
   r->host_tiles = 0;
@@ -158,6 +231,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
     if (bat->num_rows > 0 && cu[0] != 0) return PA_ERR_INVALID_ARG;
     if (cu[bat->num_rows] != bat->total_q) return PA_ERR_INVALID_ARG;
     const int bm = r->pf_bm;
+    std::vector<int> k_ends;  // key count of every prefill work item
     for (int b = 0; b < bat->num_rows; ++b) {
       const int qb = cu[b + 1] - cu[b];
       const int L = lens[b];
@@ -170,17 +244,24 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
         r->host_slots += qb;
       } else if (qb > 0) {
         const int nmb = (qb * r->g + bm - 1) / bm;
-        if (r->pf_cut > 1) {
-          for (int m = 0; m < nmb; ++m) {
-            const int r_last = std::min((m + 1) * bm, qb * r->g) - 1;
-            int per;
-            r->host_tiles += std::max(
-                1, pf_part_count(std::min(L, L - qb + r_last / r->g + 1), r->pf_cut, &per));
-          }
-        } else {
-          r->host_tiles += nmb;
+        for (int m = 0; m < nmb; ++m) {
+          const int r_last = std::min((m + 1) * bm, qb * r->g) - 1;
+          k_ends.push_back(std::min(L, L - qb + r_last / r->g + 1));
         }
       }
+    }
+    // a part count chosen per call: only without decode rows, which run
+    // beside the prefill on the same SMs and take a share the count
+    // cannot see
+    if (r->pf_auto && (r->tc2 || r->tc) && entry != E_DECODE && r->host_slots == 0) {
+      const int K = choose_parts(k_ends, r->hkv, sm_count());
+      r->pf_cut = K > 1 ? K : 0;
+      r->pf_min_units = PF_AUTO_UNITS;
+    }
+    for (int k : k_ends) {
+      int per;
+      r->host_tiles +=
+          r->pf_cut > 1 ? std::max(1, pf_part_count(k, r->pf_cut, r->pf_min_units, &per)) : 1;
     }
   }
   return check_device();
@@ -223,6 +304,7 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.tokenwise = r.tokenwise;
   a.n_slots = nullptr;
   a.pf_parts = r.pf_cut;
+  a.pf_min_units = r.pf_min_units;
   a.pf_ml = reinterpret_cast<float2*>(base + w.pf_ml);
   a.pf_acc = reinterpret_cast<float*>(base + w.pf_acc);
   return a;

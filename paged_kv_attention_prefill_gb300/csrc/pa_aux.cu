@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
       for (int m = 0; m < nmb; ++m) {
         int per;
         const int r_last = min((m + 1) * bm, qb * p.g) - 1;
-        nt += max(1, pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per));
+        const int k_end = min(L, L - qb + r_last / p.g + 1);
+        nt += max(1, pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per));
       }
     }
     const int ns = dec ? qb : 0;
@@ -98,8 +99,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
         for (int m = nmb - 1; m >= 0; --m) {
           int per;
           const int r_last = min((m + 1) * bm, qb * p.g) - 1;
-          const int parts =
-              max(1, pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per));
+          const int k_end = min(L, L - qb + r_last / p.g + 1);
+          const int parts = max(1, pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per));
           for (int c = 0; c < parts; ++c, ++k)
             if (k < max_tiles) tiles[k] = make_int2(b, m | (c << 24));
         }
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const AttnArgs a, int mixed,
       int work = max(0, min(L, L - qb + r_last / p.g + 1));
       if (a.pf_parts > 1) {
         int per;
-        if (pf_part_count(work, a.pf_parts, &per) > 1)
+        if (pf_part_count(work, a.pf_parts, a.pf_min_units, &per) > 1)
           work = min(work - c * per * PF_UNIT, per * PF_UNIT);
       }
       if (t.x >= (1 << 20) || mb >= (1 << 14) || c >= 16) s_bad = 1;
@@ -324,7 +325,8 @@ __global__ void __launch_bounds__(64) pf_merge_kernel(const AttnArgs a, int bm, 
   const int mb = R / bm;
   const int r_last = min((mb + 1) * bm, M) - 1;
   int per;
-  const int parts = pf_part_count(min(L, L - qb + r_last / p.g + 1), a.pf_parts, &per);
+  const int k_end = min(L, L - qb + r_last / p.g + 1);
+  const int parts = pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per);
   if (parts <= 1) return;  // written by the prefill kernel itself
 
   const float2* ml = a.pf_ml + ((int64_t)t * p.hq + h) * a.pf_parts;

@@ -63,26 +63,28 @@ constexpr int PF_BM = 64;       // GQA-packed query rows per prefill CTA (mma.sy
 // cut into whole-tile ranges merged by log-sum-exp).  A work item's keys
 // [0, k_end) are counted in units of PF_UNIT keys (a multiple of every
 // prefill key tile) and cut into at most `max_parts` parts of equal whole
-// units, one part per PF_PART_UNITS units or fewer: the cut depends on k_end
-// alone, so a row's result never depends on the rest of the batch, the page
-// size or the physical pages.
+// units (the last takes the rest), each of at least `min_units` units.  With
+// a fixed part count the cut depends on k_end alone, so a row's result never
+// depends on the rest of the batch, the page size or the physical pages.
 constexpr int PF_UNIT = 128;
-constexpr int PF_PART_UNITS = 128;   // 16384 keys
+constexpr int PF_PART_UNITS = 128;   // 16384 keys: least part for a part count the caller fixes
+constexpr int PF_AUTO_UNITS = 8;     // 1024 keys: least part for a count chosen per call
+constexpr int PF_AUTO_MAX = 4;       // the most parts a count chosen per call takes
 constexpr int PF_MAX_PARTS = 16;
 
 WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g,
                           int pf_parts);
 
 // Parts of a work item whose rows see keys [0, k_end): sets the units per
-// part (the last part takes the remainder) and returns the part count (0 for
-// k_end <= 0, 1 when not cut).
-__host__ __device__ inline int pf_part_count(int k_end, int max_parts, int* per_units) {
+// part and returns the part count (0 for k_end <= 0, 1 when not cut).
+__host__ __device__ inline int pf_part_count(int k_end, int max_parts, int min_units,
+                                             int* per_units) {
   if (k_end <= 0) {
     *per_units = 0;
     return 0;
   }
   const int n_u = (k_end + PF_UNIT - 1) / PF_UNIT;
-  int parts = max_parts > 1 ? (n_u + PF_PART_UNITS - 1) / PF_PART_UNITS : 1;
+  int parts = max_parts > 1 ? (n_u + min_units - 1) / min_units : 1;
   if (parts > max_parts) parts = max_parts;
   if (parts < 1) parts = 1;
   const int per = (n_u + parts - 1) / parts;
@@ -122,6 +124,7 @@ struct AttnArgs {
   const int2* tiles;         // prefill work list: (row, m-block | part << 24)
   const uint32_t* n_tiles;   // its length (device)
   int pf_parts;              // prefill key-range parts per work item at most (<= 1: not cut)
+  int pf_min_units;          // least PF_UNIT units per part
   float* pf_acc;             // partial states of cut work items
   float2* pf_ml;
   int max_decode_q;

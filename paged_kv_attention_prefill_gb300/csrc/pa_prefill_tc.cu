@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(384, 1)
   const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
   // the item's key range [k0, k1): the whole range, or one part of it
   int per_u;
-  const bool cut = pf_part_count(k_end, a.pf_parts, &per_u) > 1;
+  const bool cut = pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per_u) > 1;
   const int k0 = cut ? part * per_u * PF_UNIT : 0;
   const int k1 = cut ? min(k_end, (part + 1) * per_u * PF_UNIT) : k_end;
   const int n_tiles = k1 > k0 ? (k1 - k0 + C::BN - 1) / C::BN : 0;

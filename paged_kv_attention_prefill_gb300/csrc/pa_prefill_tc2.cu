@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
   // The item's key range [k0, k1): the whole range, or one part of it
   int per_u;
   const int k_item = k_end_of(R0, 2 * C::BM);
-  const bool cut = pf_part_count(k_item, a.pf_parts, &per_u) > 1;
+  const bool cut = pf_part_count(k_item, a.pf_parts, a.pf_min_units, &per_u) > 1;
   const int k0 = cut ? part * per_u * PF_UNIT : 0;
   const int k1 = cut ? min(k_item, (part + 1) * per_u * PF_UNIT) : k_item;
   // key tiles of each query tile in the range (0 for an empty tile B)

@@ -171,10 +171,17 @@ def test_prefill_parts_workspace_and_checks(lib):
         grown = pa.workspace_size(params(prefill_kv_parts=k), 8, 1000) - base
         states = 1000 * 16 * k * (128 + 2) * 4
         assert states <= grown <= states + 1000 * 16 * k * 8 + 64 * 1024
-    for bad in (-1, 17):
+    for bad in (-2, 17):
         assert lib.paged_attn_workspace_size(ctypes.byref(params(prefill_kv_parts=bad)), 4, 4) == 0
         for name in ENTRIES:
             assert FakeCall(lib, params(prefill_kv_parts=bad), [1, 1], [10, 20])(name) == INVALID
+    # the count chosen per call: the workspace holds 4 parts; -2 is refused
+    assert pa.workspace_size(params(prefill_kv_parts=pa.PA_PREFILL_PARTS_AUTO), 8, 1000) == \
+        pa.workspace_size(params(prefill_kv_parts=4), 8, 1000)
+    assert lib.paged_attn_workspace_size(ctypes.byref(params(prefill_kv_parts=-2)), 4, 4) == 0
+    for name in ENTRIES:
+        assert FakeCall(lib, params(prefill_kv_parts=-2), [1, 1], [10, 20])(name) == INVALID
+        assert FakeCall(lib, params(prefill_kv_parts=-1), [1, 1], [10, 20])(name) in (OK, NO_DEVICE)
     # decode never cuts prefill items: its workspace need is the uncut one
     p = params(prefill_kv_parts=8)
     c = FakeCall(lib, p, [1, 1], [10, 20], ws_bytes=pa.workspace_size(params(), 2, 2))

@@ -163,3 +163,35 @@ def test_mixed_workload_with_parts():
         del gpu
         torch.cuda.empty_cache()
     assert bitwise(outs[896], outs[784])
+
+
+def _run_auto(entry, b, host=True):
+    return run(entry, b, parts=pa.PA_PREFILL_PARTS_AUTO, host=host)
+
+
+def test_auto_part_count_on_the_long_chunk():
+    # the 2048-token chunk after 150,000 keys (d = 256, 384 equal CTAs = 2.5
+    # waves on 152 SMs): the count chosen per call cuts it in 3 (the fewest
+    # finish-time CTA waves), which equals the explicit 3-part cut here
+    gpu = workloads.make_workload(3, device="cuda", data_device="cuda", page_size=784)
+    row = workloads.sub_batch(gpu, [0], device="cuda")
+    auto = _run_auto("prefill", row)
+    assert bitwise(auto, run("prefill", row, parts=3))
+    assert not bitwise(auto, run("prefill", row, parts=0))
+    toks = [0, 1, 1000, 2047]
+    ref = oracle.paged_attention(tokens=toks, **workloads.sub_batch(gpu, [0]).oracle_args())
+    assert err(auto[toks], ref) <= TOL["f16"]
+    # with decode rows beside it (the mixed call) or without host mirrors,
+    # nothing is cut
+    assert bitwise(_run_auto("mixed", gpu), run("mixed", gpu, parts=0))
+    assert bitwise(_run_auto("prefill", row, host=False), run("prefill", row, parts=0))
+    del gpu, row
+    torch.cuda.empty_cache()
+
+
+def test_auto_part_count_leaves_many_waves_alone():
+    # the varlen prefill batch runs 960 CTAs (6.3 waves): not cut
+    gpu = workloads.make_workload(2, device="cuda", data_device="cuda")
+    assert bitwise(_run_auto("prefill", gpu), run("prefill", gpu, parts=0))
+    del gpu
+    torch.cuda.empty_cache()
