@@ -482,14 +482,16 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
       return PA_ERR_CUDA;
     dst = aux->st;
   }
+  // the prefill grid is submitted first, so its CTAs take the SMs and the
+  // decode rows' CTAs fill the SMs its last wave leaves idle
+  e = run_prefill(a, r, grid, 1, st);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
   if (max_q > 0) {
     e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(workspace, batch, r),
                    dst);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (aux && cudaEventRecord(aux->join, aux->st) != cudaSuccess) return PA_ERR_CUDA;
-  e = run_prefill(a, r, grid, 1, st);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
   if (aux && cudaStreamWaitEvent(st, aux->join, 0) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
