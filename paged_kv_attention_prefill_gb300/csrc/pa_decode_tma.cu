@@ -98,12 +98,6 @@ __device__ __forceinline__ uint32_t seg_off(int key, int seg) {
   return (uint32_t)((seg >> 3) * 2048 + key * 128 + (((seg & 7) ^ (key & 7)) << 4));
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // 8x8 transpose of 16-bit elements across the warp: lane (g, t) gives
 // M[g][2t..2t+1] and receives M[2t][g], M[2t+1][g].
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {

@@ -72,19 +72,6 @@ struct TcCfg {
   static_assert(NBAR * 8 <= 192, "barrier area");
 };
 
-// 2^x on the MUFU unit (approximate, flushes subnormal results to zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 template <int N>
 __device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&v)[N]);
 template <>
@@ -94,10 +81,6 @@ __device__ __forceinline__ void tmem_st_row<32>(uint32_t taddr, const uint32_t (
 template <>
 __device__ __forceinline__ void tmem_st_row<16>(uint32_t taddr, const uint32_t (&v)[16]) {
   tmem_st_x16(taddr, v);
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 template <int N>
