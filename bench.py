@@ -50,10 +50,10 @@ L2_BYTES = 129 * 1024 * 1024
 # Reported only while the kernel's sources are the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "ca6e0fd53d0588174a82325b24677de60d0f5c76c47f14497ba392b24e84b523",
-        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "b118652fb223ae088defcdb22930b457bfd73b3d16884163b65a6288e74fcdb2",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "83c1a930af3249858d381673482eb0e52f79bdc9d5646544c1e70a5f9ce38ad8",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "6663b84aea70173d8ba6c643859ad0003b867158a4fe7b016a1233c99a9fe659",
     },
-    "bytes_per_launch": 957533184 + 54020352,
+    "bytes_per_launch": 960341504 + 53906176,
 }
 
 
