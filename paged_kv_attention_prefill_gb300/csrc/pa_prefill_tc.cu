@@ -1,32 +1,33 @@
-// Varlen causal paged prefill on the tcgen05 tensor cores (sm_103a).
+// Varlen causal paged prefill on the tcgen05 tensor cores (sm_103a), head
+// dim 256.
 //
 // Computes the same attention as every other path of the library (the
 // packed-varlen interface with one block table per row and bottom-right
 // causal alignment, GQA, online softmax over key tiles: vllm-rlt PR #128,
-// "Purpose", prefill bullets), restructured for Blackwell:
+// "Purpose", prefill bullets), laid out for d = 256, where TMEM holds one
+// query tile's O (256 columns) next to little else:
 //
-//  * A CTA owns 128 GQA-packed query rows of one (row, KV head) -- the
-//    query heads that share the KV head stacked into the tile's M dimension
-//    (1Cat-vLLM PR #1279, commit 1) -- so each K/V tile read from HBM serves
-//    all g heads of the group.
-//  * Warp 0 (producer) gathers K/V tiles one 16-token page slot at a time
-//    with TMA (3-D tensor maps over [tokens, Hkv, d], 128-byte swizzle)
-//    straight from the block table into a multi-stage shared-memory ring;
-//    the page size only changes which token coordinate a slot starts at
-//    (1Cat-vLLM PR #616, original description: any page size that is a
-//    multiple of 16).  The slot that holds the row's last key is copied by
-//    hand with the keys past the row's end zero-filled, so no stale or
-//    poisoned cache bytes ever reach the value product.
-//  * Warp 1, one elected thread, issues tcgen05.mma: S = Q K^T (M=128,
-//    N = key tile, K = d) into one of two TMEM buffers, and O += P V
-//    (N = d, P read from TMEM) into a TMEM accumulator.  Commits signal the
-//    other warps.
-//  * Warps 4-11, two warpgroups sharing each query row (TMEM lane) by
-//    columns, read S from TMEM, apply the causal mask, run the online
-//    softmax, write P (16-bit) back into TMEM as the A operand of the second
-//    MMA (no shared-memory round trip), rescale O in TMEM when the running
-//    maximum grows by more than 2^8 (otherwise the stale maximum is kept: the
-//    final O / l is unchanged), and finally normalise O and store the rows.
+//  * A CTA owns 128 GQA-packed query rows of one (row, KV head) -- the query
+//    heads that share the KV head stacked into the MMA's M dimension
+//    (1Cat-vLLM PR #1279, commit 1).
+//  * Q lives in TMEM (128 columns of 16-bit pairs) as the A operand of
+//    S = Q K^T, which leaves room for 128-key S tiles: an N = 128 MMA runs at
+//    the full tensor rate, an N = 64 one at about two thirds of it.  TMEM:
+//    S 128 columns (P written over it), O 256, Q 128.
+//  * Warp 0 streams K tiles (128 keys, two stages) and warp 2 V half tiles
+//    (64 keys, three stages) with TMA, one box per 16-token page slot
+//    straight from the block table (1Cat-vLLM PR #616, original description:
+//    any page size that is a multiple of 16); the slot holding the row's last
+//    key is copied by hand with the keys past the row's end zero-filled.
+//  * Warp 1, one thread, issues per key tile j: S(j) once the previous P V
+//    product is done (P sits in S's columns), then O += P(j) V once P(j) is
+//    written.
+//  * Warps 4-11, two warpgroups sharing each query row (TMEM lane) by key
+//    columns, read S, mask, swap their partial row maxima through S columns
+//    both have already read, run the online softmax, write P (16-bit) over
+//    the S they read, rescale O in TMEM only when a row's maximum grows by
+//    more than 2^8, and finally normalise O and store their halves of the
+//    rows.
 //
 // Every wait is bounded (about two seconds); a CTA that runs out sets a
 // workspace flag, drains its own copies and MMAs, frees TMEM and exits.
@@ -42,84 +43,49 @@ namespace {
 
 using namespace sm100;
 
-template <int D>
 struct TcCfg {
-  static constexpr int BM = 128;                    // query rows per CTA = TMEM lanes
-  static constexpr int BN = D == 256 ? 64 : 128;    // keys per tile
-  // K is released as soon as S = Q K^T is done, V only after O += P V, so
-  // the K ring runs further ahead than the V ring.
-  static constexpr int KS = D == 64 ? 4 : (D == 128 ? 3 : 2);
-  static constexpr int VS = D == 64 ? 4 : 3;
-  static constexpr int NCH = D / 64;                // 128-byte column chunks of d
-  static constexpr int SLOTS = BN / 16;             // 16-token page slots per key tile
-  static constexpr uint32_t Q_BYTES = BM * D * 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;  // K (or V) of one tile
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
-  static constexpr uint32_t SMEM = OFF_BAR + 256 + 1024;  // barriers, alignment slack
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                      // query rows per CTA = TMEM lanes
+  static constexpr int BN = 128;                      // keys per S tile
+  static constexpr int HB = 64;                       // keys per V stage (half a tile)
+  static constexpr int KS = 2, VS = 3;                // K tile stages, V half stages
+  static constexpr int NCH = D / 64;                  // 128-byte column chunks of d
+  static constexpr uint32_t K_BYTES = BN * D * 2;     // K of one tile: [chunk][128 keys][128 B]
+  static constexpr uint32_t V_BYTES = HB * D * 2;     // V of a half tile: [chunk][64 keys][128 B]
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + KS * K_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * V_BYTES;
+  static constexpr uint32_t BAR_AREA = 192;           // mbarriers, then TMEM address and flags
+  static constexpr uint32_t SMEM = OFF_BAR + BAR_AREA + 16 + 1024;  // alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t O_COL = 2 * BN;         // S double buffer in [0, 2 BN)
-  static constexpr uint32_t P_COL = O_COL + D;      // P (16-bit pairs): BN / 2 columns
-  static constexpr uint32_t XCH_COL = 448;          // 6 spare columns: softmax warpgroups' swaps
+  static constexpr uint32_t O_COL = BN;               // S in [0, BN), P over its first BN / 2
+  static constexpr uint32_t Q_COL = O_COL + D;
   // barrier indices
   static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
-                       B_SF = 2 * KS + 2 * VS, B_SE = B_SF + 2, B_PF = B_SE + 2, B_PV = B_PF + 1,
-                       B_Q = B_PV + 1, B_DRAIN = B_Q + 1, NBAR = B_DRAIN + 1;
-  static_assert(P_COL + BN / 2 <= XCH_COL && XCH_COL + 6 <= TMEM_COLS, "TMEM budget");
+                       B_SF = 2 * KS + 2 * VS,        // S(j) written
+      B_PF = B_SF + 1,                                // P(j) written (8 warps)
+      B_PV = B_PF + 1,                                // O += P(j) V done
+      B_Q = B_PV + 1,                                 // Q in TMEM (8 warps)
+      B_DRAIN = B_Q + 1, NBAR = B_DRAIN + 1;
+  static_assert(Q_COL + D / 2 == TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(NBAR * 8 <= 192, "barrier area");
+  static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
 };
 
-template <int N>
-__device__ __forceinline__ void tmem_st_row(uint32_t taddr, const uint32_t (&v)[N]);
-template <>
-__device__ __forceinline__ void tmem_st_row<32>(uint32_t taddr, const uint32_t (&v)[32]) {
-  tmem_st_x32(taddr, v);
-}
-template <>
-__device__ __forceinline__ void tmem_st_row<16>(uint32_t taddr, const uint32_t (&v)[16]) {
-  tmem_st_x16(taddr, v);
-}
-
-template <int N>
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&x)[N]);
-template <>
-__device__ __forceinline__ void tmem_ld_row<32>(uint32_t taddr, float (&x)[32]) {
-  uint32_t r[32];
-  tmem_ld_x32(taddr, r);
-#pragma unroll
-  for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(r[k]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld_row<128>(uint32_t taddr, float (&x)[128]) {
-  uint32_t r[128];
-  tmem_ld_x128(taddr, r);
-#pragma unroll
-  for (int k = 0; k < 128; ++k) x[k] = __uint_as_float(r[k]);
-}
-template <>
-__device__ __forceinline__ void tmem_ld_row<64>(uint32_t taddr, float (&x)[64]) {
-  uint32_t r[64];
-  tmem_ld_x64(taddr, r);
-#pragma unroll
-  for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(r[k]);
-}
-
-template <typename T, int D>
+template <typename T>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
-  using C = TcCfg<D>;
+  using C = TcCfg;
+  constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + C::OFF_Q, sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V;
   const uint32_t bar0 = base + C::OFF_BAR;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 196);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::BAR_AREA);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::BAR_AREA + 4);
   auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
   const Problem& p = a.p;
@@ -162,13 +128,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_VF + s), 1);
       mbar_init(bar(C::B_VE + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_SF + s), 1);
-      mbar_init(bar(C::B_SE + s), 256);
-    }
-    mbar_init(bar(C::B_PF), 256);
+    mbar_init(bar(C::B_SF), 1);
+    mbar_init(bar(C::B_PF), 8);
     mbar_init(bar(C::B_PV), 1);
-    mbar_init(bar(C::B_Q), 128);
+    mbar_init(bar(C::B_Q), 8);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -183,9 +146,13 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 || warp == 2) {
-    // ============== producers: warp 0 streams K tiles, warp 2 V tiles ========
+    // ============== producers: warp 0 streams K tiles, warp 2 V halves =======
+    // Unit u of a producer: a K tile of BN keys (warp 0) or a V half tile of
+    // HB keys (warp 2), each a run of 16-token page slots.
     const bool isK = warp == 0;
     const int NS = isK ? C::KS : C::VS;
+    const int UK = isK ? C::BN : C::HB;                 // keys per unit
+    const uint32_t UB = isK ? C::K_BYTES : C::V_BYTES;  // bytes per unit
     const int B_FULL = isK ? C::B_KF : C::B_VF, B_EMPTY = isK ? C::B_KE : C::B_VE;
     const uint32_t ring = isK ? sK : sV;
     const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
@@ -193,20 +160,22 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) tma_prefetch_desc(tmap);
     const int P = p.page_size;
     const int64_t bt_row = (int64_t)b * p.max_pages;
-    int j = 0;
+    const int n_units = isK ? n_tiles : 2 * n_tiles;
+    int u = 0;
     bool ok = true;
-    for (; j < n_tiles; ++j) {
-      const int st = j % NS;
-      if (j >= NS) ok = mbar_wait(bar(B_EMPTY + st), ((j / NS) - 1) & 1, abort_flag, p.err);
+    for (; u < n_units; ++u) {
+      const int st = u % NS;
+      if (u >= NS) ok = mbar_wait(bar(B_EMPTY + st), ((u / NS) - 1) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      const int kbase = k0 + j * C::BN;
-      const uint32_t dst = ring + st * C::KV_BYTES;
+      const int kbase = k0 + u * UK;
+      const uint32_t dst = ring + st * UB;
+      const int slots = UK / 16;
       // slot `lane`: 1 = whole slot by TMA, 2 = partial (copied by hand), 3 = zero-fill
       int kind = 0, tok0 = 0;
-      if (lane < C::SLOTS) {
+      if (lane < slots) {
         const int s0 = kbase + 16 * lane;
         if (s0 >= L) {
           kind = 3;
@@ -238,7 +207,7 @@ __global__ void __launch_bounds__(384, 1)
             v = __ldg(reinterpret_cast<const uint4*>(src));
           }
           const int row = 16 * s + rr;
-          st_shared_v4(dst + c * (C::BN * 128) + row * 128 + ((piece ^ (row & 7)) << 4), v);
+          st_shared_v4(dst + c * (UK * 128) + row * 128 + ((piece ^ (row & 7)) << 4), v);
         }
       }
       fence_proxy_async_smem();
@@ -249,14 +218,14 @@ __global__ void __launch_bounds__(384, 1)
       if (kind == 1) {
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(dst + c * (C::BN * 128) + lane * 16 * 128, tmap, c * 64, kh, tok0,
+          tma_load_3d(dst + c * (UK * 128) + lane * 16 * 128, tmap, c * 64, kh, tok0,
                       bar(B_FULL + st));
       }
     }
     if (!ok) {
       // copies this warp started may still be landing: wait for them
-      for (int jj = max(0, j - NS); jj < j; ++jj)
-        mbar_drain(bar(B_FULL + jj % NS), (jj / NS) & 1, p.err);
+      for (int uu = max(0, u - NS); uu < u; ++uu)
+        mbar_drain(bar(B_FULL + uu % NS), (uu / NS) & 1, p.err);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer (one thread) =======================
@@ -266,46 +235,44 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
       bool ok = n_tiles == 0 || mbar_wait(bar(C::B_Q), 0, abort_flag, p.err);
       if (ok) tc_fence_after();
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int st = j % C::KS;
-          ok = mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err);
-          const int buf = j & 1;
-          if (ok && j >= 2) ok = mbar_wait(bar(C::B_SE + buf), ((j >> 1) - 1) & 1, abort_flag, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t dS = tmem + buf * C::BN;
-          // descriptors of the first step; later steps add their byte offset
-          // (>> 4) to the start-address field, which never carries out of it
-          // (the issue cost of these short MMAs is on the critical path)
-          const uint64_t a0 = sdesc_sw128(sQ, 16, 1024);
-          const uint64_t b0 = sdesc_sw128(sK + st * C::KV_BYTES, 16, 1024);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        // S(j) = Q K(j)^T: A = Q from TMEM (16 head-dim columns = 8 columns
+        // of 16-bit pairs per step); it overwrites P(j-1), so the previous
+        // P V product must be done
+        const int st = j % C::KS;
+        ok = mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err);
+        if (ok && j >= 1) ok = mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t b0 = sdesc_sw128(sK + st * C::K_BYTES, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint64_t ad = a0 + (uint64_t)(((k >> 2) * (C::BM * 128) + (k & 3) * 32) >> 4);
-            const uint64_t bd = b0 + (uint64_t)(((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4);
-            tc_mma_f16(dS, ad, bd, idS, k > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(C::B_SF + buf));
-          tc_commit(bar(C::B_KE + st));
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t bd = b0 + (uint64_t)(((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4);
+          tc_mma_f16_ts(tmem, tmem + C::Q_COL + 8 * k, bd, idS, k > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int jj = j - 1, stp = jj % C::VS;
-          ok = mbar_wait(bar(C::B_VF + stp), (jj / C::VS) & 1, abort_flag, p.err);
-          if (ok) ok = mbar_wait(bar(C::B_PF), jj & 1, abort_flag, p.err);
+        tc_commit(bar(C::B_SF));
+        tc_commit(bar(C::B_KE + st));
+        // O += P(j) V(j), V in two half tiles of HB keys
+        ok = mbar_wait(bar(C::B_PF), j & 1, abort_flag, p.err);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = 2 * j + h, sv = q % C::VS;
+          if (ok) ok = mbar_wait(bar(C::B_VF + sv), (q / C::VS) & 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t v0 = sdesc_sw128(sV + stp * C::KV_BYTES, C::BN * 128, 1024);
+          const uint64_t v0 = sdesc_sw128(sV + sv * C::V_BYTES, C::HB * 128, 1024);
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k) {
-            // A = P straight from TMEM: 16 keys = 8 columns of 16-bit pairs
+          for (int k = 0; k < C::HB / 16; ++k) {
+            // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
             const uint64_t bd = v0 + (uint64_t)((k * 16 * 128) >> 4);
-            tc_mma_f16_ts(tmem + C::O_COL, tmem + C::P_COL + 8 * k, bd, idO,
-                          (jj > 0 || k > 0) ? 1u : 0u);
+            tc_mma_f16_ts(tmem + C::O_COL, tmem + (h * (C::HB / 16) + k) * 8, bd, idO,
+                          (j > 0 || h > 0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(bar(C::B_PV));
-          tc_commit(bar(C::B_VE + stp));
         }
+        if (!ok) break;
+        tc_commit(bar(C::B_PV));
+        tc_commit(bar(C::B_VE + (2 * j) % C::VS));
+        tc_commit(bar(C::B_VE + (2 * j + 1) % C::VS));
       }
       // nothing this thread issued may still run once TMEM is freed
       tc_commit(bar(C::B_DRAIN));
@@ -313,15 +280,12 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ============ softmax / correction / epilogue ==============================
-    // Two warpgroups share every tile row (TMEM lane): warpgroup hf (warps
-    // 4-7: hf = 0, warps 8-11: hf = 1) owns columns [hf BN/2, (hf+1) BN/2) of
-    // S and P and head-dim columns [hf d/2, (hf+1) d/2) of O.  Each tile they
-    // swap their partial row maxima through spare TMEM columns and a named
-    // barrier (so both take identical rescale decisions); each keeps its own
-    // partial row sum, added in a fixed order at the end.  This loop never
-    // leaves early: after a timed-out wait it runs on (flag raised, waits
-    // return at once) so both warpgroups always meet the same barriers.
+    // ============ Q, softmax, epilogue =========================================
+    // Warpgroup hf (warps 4-7: hf = 0, warps 8-11: hf = 1) owns key columns
+    // [hf BN/2, (hf+1) BN/2) of each S tile and head-dim columns [hf d/2,
+    // (hf+1) d/2) of Q and of O.  The loop never leaves early: after a
+    // timed-out wait it runs on (flag raised, waits return at once), so both
+    // warpgroups always meet the same barriers.
     constexpr int HN = C::BN / 2, HD = D / 2;
     const int hf = warp >= 8 ? 1 : 0;
     const int q4 = warp & 3;          // TMEM lane quarter this warp may access
@@ -329,57 +293,67 @@ __global__ void __launch_bounds__(384, 1)
     const int R = R0 + r;
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
-    const int last = valid ? L - qb + i : -1;  // last visible key of this row
+    const int last = valid ? L - qb + i - k0 : -1 - k0;  // last visible key, from k0
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
-    if (hf == 0) {
-      const T* qrow = static_cast<const T*>(a.q) + qoff;
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-#pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          const uint4 v = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + pc * 8))
-                                : make_uint4(0u, 0u, 0u, 0u);
-          st_shared_v4(sQ + c * (C::BM * 128) + r * 128 + ((pc ^ (r & 7)) << 4), v);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_Q));
-    }
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    {
+      // this warpgroup's half of the row's Q into TMEM (16-bit pairs)
+      const T* qrow = static_cast<const T*>(a.q) + qoff + hf * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint4 u = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + w * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * w] = u.x;
+          v[4 * w + 1] = u.y;
+          v[4 * w + 2] = u.z;
+          v[4 * w + 3] = u.w;
+        }
+        tmem_st_x32(trow + C::Q_COL + hf * (HD / 2) + c * 32, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_Q));
+    }
     const float sl2 = p.sl2;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < n_tiles; ++j) {
-      const int buf = j & 1;
-      mbar_wait(bar(C::B_SF + buf), (j >> 1) & 1, abort_flag, p.err);
+      mbar_wait(bar(C::B_SF), j & 1, abort_flag, p.err);
       tc_fence_after();
+      // S(j) was issued after the previous P V product completed: O is stable
       float x[HN];
-      tmem_ld_row<HN>(trow + buf * C::BN + hf * HN, x);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_SE + buf));
-
-      const int kb = k0 + j * C::BN + hf * HN;
+      float mt;  // max raw logit of this half tile (masked keys -> -inf)
+      {
+        uint32_t u[HN];
+        mt = tmem_ld_red_max_x64(trow + hf * HN, u);  // the load also returns the max
+#pragma unroll
+        for (int k = 0; k < HN; ++k) x[k] = __uint_as_float(u[k]);
+      }
+      const int kb = j * C::BN + hf * HN;
       if (kb + HN - 1 > last) {
 #pragma unroll
         for (int k = 0; k < HN; ++k)
           if (kb + k > last) x[k] = -INFINITY;
-      }
-      float mt = -INFINITY;  // max raw logit of this half tile (masked keys -> -inf)
-      {
         float pm[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) pm[u] = x[u];
 #pragma unroll
         for (int k = 8; k < HN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mt = fmaxf(mt, pm[u]);
+        mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
-      {  // swap partial maxima with the other warpgroup
+      {
+        // swap partial maxima through the last S column of each half, which
+        // both have read (hf = 0: column 63, which the other warpgroup reads
+        // before writing its P there; hf = 1: column 127, which no P covers)
         uint32_t v[1] = {__float_as_uint(mt)};
-        tmem_st_x1(trow + C::XCH_COL + 2 * buf + hf, v);
+        tmem_st_x1(trow + hf * HN + HN - 1, v);
         tc_fence_before();
         named_bar_sync(1, 256);
         tc_fence_after();
-        tmem_ld_x1(trow + C::XCH_COL + 2 * buf + (hf ^ 1), v);
+        tmem_ld_x1(trow + (hf ^ 1) * HN + HN - 1, v);
         mt = fmaxf(mt, __uint_as_float(v[0]));
       }
       const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
@@ -393,18 +367,6 @@ __global__ void __launch_bounds__(384, 1)
         m_used = m_new;
       }
       const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
-#pragma unroll
-      for (int k = 0; k < HN; ++k) {
-        x[k] = ex2(fmaf(x[k], sl2, nmu));
-        ps[k & 7] += x[k];
-      }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // the previous tile's P V must be done: O is stable and P's buffer free
-      if (j >= 1) {
-        mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
-        tc_fence_after();
-      }
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
@@ -415,32 +377,41 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st_x32(trow + C::O_COL + hf * HD + c * 32, o);
         }
       }
-      l = l * factor + rs;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+#pragma unroll
+      for (int k = 0; k < HN; ++k) {
+        x[k] = ex2(fmaf(x[k], sl2, nmu));
+        ps[k & 7] += x[k];
+      }
       {
-        // P (16-bit pairs) into TMEM: this warpgroup's HN keys = HN / 2 columns
+        // P (16-bit pairs) over this warpgroup's keys: HN / 2 columns at the
+        // start of S, then one arrival per warp
         uint32_t pk[HN / 2];
 #pragma unroll
         for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
-        tmem_st_row<HN / 2>(trow + C::P_COL + hf * (HN / 2), pk);
+        tmem_st_x32(trow + hf * (HN / 2), pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PF));
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PF));
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l = l * factor + rs;
     }
-    // ---- epilogue: out = O / (l_0 + l_1) * v_scale ----
+    // ---- epilogue: out = O / (l_0 + l_1) * v_scale, or this part's state ----
+    float lt = 0.f;
     if (n_tiles > 0) {
       mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
       tc_fence_after();
-    }
-    float lt;
-    {
+      // the partial row sums, swapped through S columns the last P V product
+      // has finished reading, added in warpgroup order
       uint32_t v[1] = {__float_as_uint(l)};
-      tmem_st_x1(trow + C::XCH_COL + 4 + hf, v);
+      tmem_st_x1(trow + hf * HN, v);
       tc_fence_before();
       named_bar_sync(1, 256);
       tc_fence_after();
-      tmem_ld_x1(trow + C::XCH_COL + 4 + (hf ^ 1), v);
+      tmem_ld_x1(trow + (hf ^ 1) * HN, v);
       const float lo = __uint_as_float(v[0]);
-      lt = hf == 0 ? l + lo : lo + l;  // the same sum in both warpgroups
+      lt = hf == 0 ? l + lo : lo + l;
     }
     T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
     if (cut) {
@@ -537,45 +508,36 @@ bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int 
 
 namespace {
 
-template <typename T, int D>
+template <typename T>
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
                       cudaStream_t st) {
-  using C = TcCfg<D>;
-  auto k = prefill_tc_kernel<T, D>;
+  auto k = prefill_tc_kernel<T>;
   static DeviceFlags attr;
   cudaError_t e = attr.once([&] {
-    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, C::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, TcCfg::SMEM, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
-  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype &&
-         (d == 64 || d == 128 || d == 256) && cache_tokens < (int64_t(1) << 31) &&
-         encode_fn() != nullptr;
+  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype && d == 256 &&
+         cache_tokens < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st) {
   if (grid_x == 0) return cudaSuccess;
+  if (a.p.d != 256) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;
   if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
       !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
-  const bool bf = q_dtype == PA_BF16;
-  switch (a.p.d) {
-    case 64: return bf ? launch_tc<__nv_bfloat16, 64>(a, tk, tv, grid_x, st)
-                       : launch_tc<__half, 64>(a, tk, tv, grid_x, st);
-    case 128: return bf ? launch_tc<__nv_bfloat16, 128>(a, tk, tv, grid_x, st)
-                        : launch_tc<__half, 128>(a, tk, tv, grid_x, st);
-    case 256: return bf ? launch_tc<__nv_bfloat16, 256>(a, tk, tv, grid_x, st)
-                        : launch_tc<__half, 256>(a, tk, tv, grid_x, st);
-  }
-  return cudaErrorInvalidValue;
+  return q_dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, tk, tv, grid_x, st)
+                            : launch_tc<__half>(a, tk, tv, grid_x, st);
 }
 
 }  // namespace pa
