@@ -272,6 +272,21 @@ def test_repeated_calls_bitwise_and_no_device_errors():
     assert pa.read_errors(ws) == 0
 
 
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (256, "bf16"), (256, "f16")])
+def test_many_key_tiles_repeated_runs_match_oracle(d, dtype):
+    # long rows over many key tiles and several query tiles per row, run
+    # repeatedly: every run within tolerance and bitwise equal to the first
+    # (guards the ordering of P stores against the P V products in flight,
+    # whose violation showed up only intermittently and only on such rows)
+    ql, kl = [200, 300, 129], [1000, 3000, 5000]
+    cpu, gpu = small(ql, kl, d=d, dtype=dtype, P=16, seed=27)
+    ref = ref_of(cpu)
+    first = run("prefill", gpu)
+    assert max_err(first, ref) <= TOL[dtype]
+    for _ in range(5):
+        assert_bitwise(run("prefill", gpu), first)
+
+
 def test_device_flags_bad_block_table_entry_without_fault():
     # the host mirrors are withheld so only the kernels can see the bad entry;
     # the kernels must not dereference it and must raise the sticky flag
