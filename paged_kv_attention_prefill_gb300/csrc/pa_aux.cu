@@ -229,6 +229,21 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
   const int h = blockIdx.y;
   if (n_slots_dev && slot >= (int)*n_slots_dev) return;
   if (slot >= n_slots) return;
+  // The 16 partial states and this thread's accumulator columns are loaded
+  // before the row lookup, so their latency overlaps it: splits past the
+  // row's last (never written: stale bytes) get weight 0 and are not read
+  // further.
+  constexpr int CPT = D / 64;  // accumulator columns per thread
+  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * NSPLIT;
+  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * NSPLIT * D;
+  float2 mlv[NSPLIT];
+  float av[CPT][NSPLIT];
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k) {
+    mlv[k] = ml[k];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) av[c][k] = acc[k * D + threadIdx.x + 64 * c];
+  }
   const int t = a.slot_tok ? a.slot_tok[slot] : slot;
   // row of token t: largest b with cu_q[b] <= t
   int lo = 0, hi = p.num_rows - 1;
@@ -246,34 +261,29 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
   const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
   const int nsp = tps ? (n_tiles + tps - 1) / tps : 0;
 
-  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * NSPLIT;
   float mstar = -INFINITY;
-  for (int k = 0; k < nsp; ++k) {
-    const float2 v = ml[k];
-    if (v.y > 0.f) mstar = fmaxf(mstar, v.x);
-  }
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k)
+    if (k < nsp && mlv[k].y > 0.f) mstar = fmaxf(mstar, mlv[k].x);
   float w[NSPLIT];
   float lsum = 0.f;
 #pragma unroll
   for (int k = 0; k < NSPLIT; ++k) {
     w[k] = 0.f;
-    if (k < nsp) {
-      const float2 v = ml[k];
-      if (v.y > 0.f) {
-        w[k] = exp2f(v.x - mstar);
-        lsum += w[k] * v.y;
-      }
+    if (k < nsp && mlv[k].y > 0.f) {
+      w[k] = exp2f(mlv[k].x - mstar);
+      lsum += w[k] * mlv[k].y;
     }
   }
   const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * NSPLIT * D;
   T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
-  for (int c = threadIdx.x; c < D; c += 64) {
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NSPLIT; ++k)
-      if (w[k] != 0.f) s += w[k] * acc[k * D + c];
-    out[c] = from_float<T>(s * inv);
+      if (w[k] != 0.f) s += w[k] * av[c][k];
+    out[threadIdx.x + 64 * c] = from_float<T>(s * inv);
   }
 }
 
