@@ -11,23 +11,27 @@
 //    heads that share the KV head stacked into the MMA's M dimension
 //    (1Cat-vLLM PR #1279, commit 1).
 //  * Q lives in TMEM (128 columns of 16-bit pairs) as the A operand of
-//    S = Q K^T, which leaves room for 128-key S tiles: an N = 128 MMA runs at
-//    the full tensor rate, an N = 64 one at about two thirds of it.  TMEM:
-//    S 128 columns (P written over it), O 256, Q 128.
+//    S = Q K^T, so the S product reads only K from shared memory (an MMA
+//    with both operands there, M = N = 128, asks for the whole shared-memory
+//    bandwidth) and S tiles have 128 keys (an N = 64 MMA runs at about two
+//    thirds of the rate).  TMEM: S 128 columns, O 256, Q 128.
+//  * P goes to shared memory (the A operand of P V), so S's columns are free
+//    as soon as the softmax holds S in registers: S(j + 1) is computed while
+//    the softmax of tile j runs.
 //  * Warp 0 streams K tiles (128 keys, two stages) and warp 2 V half tiles
-//    (64 keys, three stages) with TMA, one box per 16-token page slot
+//    (64 keys, two stages) with TMA, one box per 16-token page slot
 //    straight from the block table (1Cat-vLLM PR #616, original description:
 //    any page size that is a multiple of 16); the slot holding the row's last
 //    key is copied by hand with the keys past the row's end zero-filled.
-//  * Warp 1, one thread, issues per key tile j: S(j) once the previous P V
-//    product is done (P sits in S's columns), then O += P(j) V once P(j) is
-//    written.
+//  * Warp 1, one thread, issues S(0), then per key tile j: S(j + 1) once the
+//    softmax has read S(j), and O += P(j) V in two 64-key halves, each once
+//    that half of P(j) is in shared memory.
 //  * Warps 4-11, two warpgroups sharing each query row (TMEM lane) by key
-//    columns, read S, mask, swap their partial row maxima through S columns
-//    both have already read, run the online softmax, write P (16-bit) over
-//    the S they read, rescale O in TMEM only when a row's maximum grows by
-//    more than 2^8, and finally normalise O and store their halves of the
-//    rows.
+//    columns, read S, mask, swap their partial row maxima through shared
+//    memory, run the online softmax and write their half of P, once the
+//    previous tile's product has read it.  O is rescaled in TMEM only when a
+//    row's maximum grows by more than 2^8, after that product is done.
+//    Finally they normalise O and store their halves of the rows.
 //
 // Every wait is bounded (about two seconds); a CTA that runs out sets a
 // workspace flag, drains its own copies and MMAs, frees TMEM and exits.
@@ -48,24 +52,30 @@ struct TcCfg {
   static constexpr int BM = 128;                      // query rows per CTA = TMEM lanes
   static constexpr int BN = 128;                      // keys per S tile
   static constexpr int HB = 64;                       // keys per V stage (half a tile)
-  static constexpr int KS = 2, VS = 3;                // K tile stages, V half stages
+  // Shared memory: K 2 x 64 KB + V 2 x 32 KB + P 32 KB + 1 KB; the K/V
+  // rings are what is left for hiding the copies' latency
+  static constexpr int KS = 2, VS = 2;                // K tile stages, V half stages
   static constexpr int NCH = D / 64;                  // 128-byte column chunks of d
   static constexpr uint32_t K_BYTES = BN * D * 2;     // K of one tile: [chunk][128 keys][128 B]
   static constexpr uint32_t V_BYTES = HB * D * 2;     // V of a half tile: [chunk][64 keys][128 B]
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KS * K_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + VS * V_BYTES;
+  static constexpr uint32_t P_BYTES = BM * BN * 2;    // P: [64-key half][128 rows][128 B]
+  static constexpr uint32_t OFF_P = OFF_V + VS * V_BYTES;
+  static constexpr uint32_t OFF_X = OFF_P + P_BYTES;  // [2][128] floats: partial maxima / sums
+  static constexpr uint32_t OFF_BAR = OFF_X + 2 * BM * 4;
   static constexpr uint32_t BAR_AREA = 192;           // mbarriers, then TMEM address and flags
   static constexpr uint32_t SMEM = OFF_BAR + BAR_AREA + 16 + 1024;  // alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t O_COL = BN;               // S in [0, BN), P over its first BN / 2
+  static constexpr uint32_t O_COL = BN;               // S in [0, BN)
   static constexpr uint32_t Q_COL = O_COL + D;
   // barrier indices
   static constexpr int B_KF = 0, B_KE = KS, B_VF = 2 * KS, B_VE = 2 * KS + VS,
                        B_SF = 2 * KS + 2 * VS,        // S(j) written
-      B_PF = B_SF + 1,                                // P(j) written (8 warps)
-      B_PV = B_PF + 1,                                // O += P(j) V done
-      B_Q = B_PV + 1,                                 // Q in TMEM (8 warps)
+      B_SC = B_SF + 1,                                // S(j) read by the softmax (8 warps)
+      B_PF = B_SC + 1,                                // [2] P(j) half h in shared memory (4 warps)
+      B_PV = B_PF + 2,                                // [2] O += P(j) V, half h, done
+      B_Q = B_PV + 2,                                 // Q in TMEM (8 warps)
       B_DRAIN = B_Q + 1, NBAR = B_DRAIN + 1;
   static_assert(Q_COL + D / 2 == TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -82,7 +92,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sP = base + C::OFF_P;
+  volatile float* xch = reinterpret_cast<volatile float*>(smem + C::OFF_X);
   const uint32_t bar0 = base + C::OFF_BAR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::BAR_AREA);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::BAR_AREA + 4);
@@ -129,8 +140,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::B_VE + s), 1);
     }
     mbar_init(bar(C::B_SF), 1);
-    mbar_init(bar(C::B_PF), 8);
-    mbar_init(bar(C::B_PV), 1);
+    mbar_init(bar(C::B_SC), 8);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(C::B_PF + h), 4);
+      mbar_init(bar(C::B_PV + h), 1);
+    }
     mbar_init(bar(C::B_Q), 8);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
@@ -233,16 +247,11 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
       constexpr uint32_t idS = idesc_f16(fmt, 128, C::BN, false);
       constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
-      bool ok = n_tiles == 0 || mbar_wait(bar(C::B_Q), 0, abort_flag, p.err);
-      if (ok) tc_fence_after();
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        // S(j) = Q K(j)^T: A = Q from TMEM (16 head-dim columns = 8 columns
-        // of 16-bit pairs per step); it overwrites P(j-1), so the previous
-        // P V product must be done
+      // S(j) = Q K(j)^T: A = Q from TMEM (16 head-dim columns = 8 columns
+      // of 16-bit pairs per step)
+      auto issue_S = [&](int j) {
         const int st = j % C::KS;
-        ok = mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err);
-        if (ok && j >= 1) ok = mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
-        if (!ok) break;
+        if (!mbar_wait(bar(C::B_KF + st), (j / C::KS) & 1, abort_flag, p.err)) return false;
         tc_fence_after();
         const uint64_t b0 = sdesc_sw128(sK + st * C::K_BYTES, 16, 1024);
 #pragma unroll
@@ -252,27 +261,42 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc_commit(bar(C::B_SF));
         tc_commit(bar(C::B_KE + st));
-        // O += P(j) V(j), V in two half tiles of HB keys
-        ok = mbar_wait(bar(C::B_PF), j & 1, abort_flag, p.err);
+        return true;
+      };
+      bool ok = n_tiles == 0 || mbar_wait(bar(C::B_Q), 0, abort_flag, p.err);
+      if (ok) tc_fence_after();
+      if (ok && n_tiles > 0) ok = issue_S(0);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        // S(j + 1) as soon as the softmax holds S(j) in registers (P goes to
+        // shared memory, so nothing else lives in S's columns)
+        if (j + 1 < n_tiles) {
+          ok = mbar_wait(bar(C::B_SC), j & 1, abort_flag, p.err);
+          if (ok) {
+            tc_fence_after();
+            ok = issue_S(j + 1);
+          }
+          if (!ok) break;
+        }
+        // O += P(j) V(j) in two halves of HB keys, each once its half of
+        // P(j) is in shared memory: A = P (K-major), B = V (N-major)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int q = 2 * j + h, sv = q % C::VS;
+          ok = mbar_wait(bar(C::B_PF + h), j & 1, abort_flag, p.err);
           if (ok) ok = mbar_wait(bar(C::B_VF + sv), (q / C::VS) & 1, abort_flag, p.err);
           if (!ok) break;
           tc_fence_after();
+          const uint64_t a0 = sdesc_sw128(sP + h * (C::BM * 128), 16, 1024);
           const uint64_t v0 = sdesc_sw128(sV + sv * C::V_BYTES, C::HB * 128, 1024);
 #pragma unroll
           for (int k = 0; k < C::HB / 16; ++k) {
-            // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
+            const uint64_t ad = a0 + (uint64_t)((k * 32) >> 4);
             const uint64_t bd = v0 + (uint64_t)((k * 16 * 128) >> 4);
-            tc_mma_f16_ts(tmem + C::O_COL, tmem + (h * (C::HB / 16) + k) * 8, bd, idO,
-                          (j > 0 || h > 0 || k > 0) ? 1u : 0u);
+            tc_mma_f16(tmem + C::O_COL, ad, bd, idO, (j > 0 || h > 0 || k > 0) ? 1u : 0u);
           }
+          tc_commit(bar(C::B_VE + sv));
+          tc_commit(bar(C::B_PV + h));
         }
-        if (!ok) break;
-        tc_commit(bar(C::B_PV));
-        tc_commit(bar(C::B_VE + (2 * j) % C::VS));
-        tc_commit(bar(C::B_VE + (2 * j + 1) % C::VS));
       }
       // nothing this thread issued may still run once TMEM is freed
       tc_commit(bar(C::B_DRAIN));
@@ -322,7 +346,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < n_tiles; ++j) {
       mbar_wait(bar(C::B_SF), j & 1, abort_flag, p.err);
       tc_fence_after();
-      // S(j) was issued after the previous P V product completed: O is stable
+      // S(j) may run while the previous P V product still does: O and P's
+      // buffer are touched only after waiting for that product
       float x[HN];
       float mt;  // max raw logit of this half tile (masked keys -> -inf)
       {
@@ -345,16 +370,16 @@ __global__ void __launch_bounds__(384, 1)
                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
       {
-        // swap partial maxima through the last S column of each half, which
-        // both have read (hf = 0: column 63, which the other warpgroup reads
-        // before writing its P there; hf = 1: column 127, which no P covers)
-        uint32_t v[1] = {__float_as_uint(mt)};
-        tmem_st_x1(trow + hf * HN + HN - 1, v);
-        tc_fence_before();
+        // swap partial maxima through shared memory; then S(j) is consumed
+        // and the next S may overwrite it.  (The next tile's write here comes
+        // after S(j + 1), which waits for every warp's arrival below, so the
+        // other warpgroup has read this value by then.)
+        xch[hf * C::BM + r] = mt;
         named_bar_sync(1, 256);
-        tc_fence_after();
-        tmem_ld_x1(trow + (hf ^ 1) * HN + HN - 1, v);
-        mt = fmaxf(mt, __uint_as_float(v[0]));
+        mt = fmaxf(mt, xch[(hf ^ 1) * C::BM + r]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_SC));
       }
       const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
       float factor = 1.f;
@@ -368,6 +393,9 @@ __global__ void __launch_bounds__(384, 1)
       }
       const float nmu = m_used == -INFINITY ? 0.f : -m_used;
       if (__any_sync(0xffffffffu, need)) {
+        // the previous P V product (its commit covers every earlier MMA)
+        mbar_wait(bar(C::B_PV + 1), (j - 1) & 1, abort_flag, p.err);
+        tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
@@ -384,35 +412,37 @@ __global__ void __launch_bounds__(384, 1)
         ps[k & 7] += x[k];
       }
       {
-        // P (16-bit pairs) over this warpgroup's keys: HN / 2 columns at the
-        // start of S, then one arrival per warp
+        // P (16-bit) of this warpgroup's keys into half hf of P's buffer
+        // (the A operand of P V: 128-byte rows, 128-byte swizzle), once the
+        // previous tile's product has read that half; one arrival per warp
         uint32_t pk[HN / 2];
 #pragma unroll
         for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
-        tmem_st_x32(trow + hf * (HN / 2), pk);
-        tc_fence_before();
+        if (j > 0) mbar_wait(bar(C::B_PV + hf), (j - 1) & 1, abort_flag, p.err);
+        const uint32_t prow = sP + hf * (C::BM * 128) + r * 128;
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc)
+          st_shared_v4(prow + ((pc ^ (r & 7)) << 4),
+                       make_uint4(pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2], pk[4 * pc + 3]));
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PF));
+        if (lane == 0) mbar_arrive(bar(C::B_PF + hf));
       }
       const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * factor + rs;
     }
     // ---- epilogue: out = O / (l_0 + l_1) * v_scale, or this part's state ----
-    float lt = 0.f;
     if (n_tiles > 0) {
-      mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
+      mbar_wait(bar(C::B_PV + 1), (n_tiles - 1) & 1, abort_flag, p.err);
       tc_fence_after();
-      // the partial row sums, swapped through S columns the last P V product
-      // has finished reading, added in warpgroup order
-      uint32_t v[1] = {__float_as_uint(l)};
-      tmem_st_x1(trow + hf * HN, v);
-      tc_fence_before();
-      named_bar_sync(1, 256);
-      tc_fence_after();
-      tmem_ld_x1(trow + (hf ^ 1) * HN, v);
-      const float lo = __uint_as_float(v[0]);
-      lt = hf == 0 ? l + lo : lo + l;
     }
+    // the partial row sums, swapped through shared memory once every read
+    // of the maxima is done, added in warpgroup order
+    named_bar_sync(1, 256);
+    xch[hf * C::BM + r] = l;
+    named_bar_sync(1, 256);
+    const float lo = xch[(hf ^ 1) * C::BM + r];
+    const float lt = hf == 0 ? l + lo : lo + l;
     T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
     if (cut) {
       // this part's unnormalised O (each warpgroup its d / 2 columns), the
