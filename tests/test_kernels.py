@@ -287,6 +287,44 @@ def test_many_key_tiles_repeated_runs_match_oracle(d, dtype):
         assert_bitwise(run("prefill", gpu), first)
 
 
+def _ramp_keys(b, growth):
+    """Scales key t of every row by (1 + growth * t / L): the logits, and with
+    them each row's running maximum, keep growing along the row.  V is
+    scaled by 1/4 (exactly): the softmax gets nearly one-hot, so outputs
+    approach single V entries, and bf16 rounds values above 4 by up to 2^-6,
+    more than the tolerance."""
+    b.v_cache.mul_(0.25)
+    P = b.k_cache.shape[1]
+    for r, L in enumerate(b.kv_lens):
+        t = torch.arange(L)
+        pages = b.block_table[r, t // P].long()
+        f = (1.0 + growth * t.double() / max(L, 1)).to(torch.float32)
+        rows = b.k_cache[pages, t % P].float() * f[:, None, None]
+        b.k_cache[pages, t % P] = rows.to(b.k_cache.dtype)
+    return b
+
+
+@pytest.mark.parametrize("d,dtype,parts", [(64, "bf16", 0), (128, "bf16", 0), (128, "f16", 2),
+                                           (256, "f16", 0), (256, "bf16", 3)])
+def test_running_maximum_growing_along_rows_rescales_o(d, dtype, parts):
+    # keys scaled up along each row, so every query's running maximum passes
+    # its exponent reference by more than 2^8 again and again over the key
+    # tiles: the lazy O rescale runs mid-row on the prefill kernels (and its
+    # ordering against the P V product in flight), in cut parts, and in the
+    # decode rows of the mixed call
+    ql, kl = [200, 1, 300, 4], [3000, 4000, 5000, 2500]
+    cpu = workloads.make_batch(ql, kl, num_q_heads=8, num_kv_heads=2, head_dim=d, page_size=16,
+                               q_dtype=dtype, seed=31)
+    cpu = _ramp_keys(cpu, 12.0)
+    gpu = cpu.to("cuda")
+    ref = ref_of(cpu)
+    kw = dict(prefill_kv_parts=parts) if parts else {}
+    first = run("mixed", gpu, **kw)
+    assert max_err(first, ref) <= TOL[dtype]
+    for _ in range(3):
+        assert_bitwise(run("mixed", gpu, **kw), first)
+
+
 def test_device_flags_bad_block_table_entry_without_fault():
     # the host mirrors are withheld so only the kernels can see the bad entry;
     # the kernels must not dereference it and must raise the sticky flag
