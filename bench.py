@@ -51,9 +51,9 @@ L2_BYTES = 129 * 1024 * 1024
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
         "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "83c1a930af3249858d381673482eb0e52f79bdc9d5646544c1e70a5f9ce38ad8",
-        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "6663b84aea70173d8ba6c643859ad0003b867158a4fe7b016a1233c99a9fe659",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "48ad9f70924798a53f893583c129da78740890cf13b315a2146acf9decea007b",
     },
-    "bytes_per_launch": 960341504 + 53906176,
+    "bytes_per_launch": 966179072 + 53469952,
 }
 
 
