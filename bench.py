@@ -318,6 +318,32 @@ def part_prefill_fp8(steps, warmup, stream, pk):
     return res
 
 
+def part_prefill_fp8_d256(steps, warmup, stream, pk):
+    """The mixed workload's 2048-token prefill row alone (d = 256) with fp16 Q
+    and an fp8 E5M2 cache (per-tensor scales 0.5 / 2.0)."""
+    import paged_kv_attention_prefill_gb300 as pa
+    full = workloads.make_workload(3, device="cuda", data_device="cuda", kv_dtype="e5m2",
+                                   k_scale=0.5, v_scale=2.0)
+    b = workloads.sub_batch(full, [0], device="cuda")
+    del full
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    out = torch.empty_like(b.q)
+    kw = call_args(b)
+
+    def fn():
+        pa.paged_attn_prefill(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                              b.seq_lens, out=out, workspace=ws, **kw)
+    ms = time_calls(fn, steps, warmup, stream)
+    F = metrics.prefill_flops(b.q_lens, b.kv_lens, b.num_q_heads, b.head_dim)
+    tf = F / (ms * 1e-3) / 1e12
+    res = {"workload": "the mixed workload's prefill row alone (2048 tokens after 150000 cached, "
+                       "24/4 heads, d=256) with fp16 Q and an fp8_e5m2 KV cache",
+           "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "frac_of_fp16_peak": round(tf / pk["bf16"], 4)}
+    del b, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def part_small1(steps, warmup, stream):
     import paged_kv_attention_prefill_gb300 as pa
     b = workloads.make_workload(1).to("cuda")
@@ -510,6 +536,7 @@ def run_ours(args):
             parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk)
             parts["mixed_chunk_plus_decode"] = part_mixed3(ps, pw, stream, pk)
             parts["prefill_fp8_cache"] = part_prefill_fp8(ps, pw, stream, pk)
+            parts["prefill_fp8_cache_d256"] = part_prefill_fp8_d256(ps, pw, stream, pk)
             parts["decode_small_4rows"] = part_small1(max(ps, 50), 5, stream)
         cpu_val, cores, sample, cpu_extra = cpu_baseline_sample(b, budget_s=args.cpu_seconds)
         res = {

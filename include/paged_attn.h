@@ -162,7 +162,7 @@ enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
  * independent of the rest of the batch, the page size and the physical
  * pages; a cut item equals the uncut one to rounding only.  Applies to the
  * tcgen05 prefill (16-bit q with a same-type cache, or an E5M2 cache at
- * head_dim 128); other prefill paths ignore it.  The workspace grows by
+ * head_dim 128 or 256); other prefill paths ignore it.  The workspace grows by
  * total_q * Hq * K * (head_dim + 2) * 4 bytes; paged_attn_decode ignores the
  * field.  Values outside 0..16 and PA_PREFILL_PARTS_AUTO return
  * PA_ERR_INVALID_ARG.

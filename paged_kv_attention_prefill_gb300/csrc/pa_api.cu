@@ -390,7 +390,7 @@ cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, in
   if (r.tc2)
     e = launch_prefill_tc2(a, r.qd, r.kvd, grid_tiles, st);
   else if (r.tc)
-    e = launch_prefill_tc(a, r.qd, grid_tiles, st);
+    e = launch_prefill_tc(a, r.qd, r.kvd, grid_tiles, st);
   else
     return launch_prefill_mma(a, r.qd, r.kvd, grid_tiles, st);
   if (e != cudaSuccess || grid_tiles == 0) return e;

@@ -152,10 +152,12 @@ cudaError_t launch_row_order(const AttnArgs& a, int32_t* order, cudaStream_t st)
 cudaError_t launch_f32(const AttnArgs& a, int decode_mode, int grid_x, int n_mblk,
                        cudaStream_t st);
 bool prefill_mma_supported(int q_dtype, int kv_dtype, int d);
-// tcgen05 prefill (16-bit q with a same-type cache, cache < 2^31 tokens)
+// tcgen05 prefill at d = 256 (16-bit q with a same-type or fp8 E5M2 cache,
+// cache < 2^31 tokens)
 constexpr int PF_BM_TC = 128;
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
-cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st);
+cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int kv_dtype, int grid_x,
+                              cudaStream_t st);
 // tcgen05 prefill with two query tiles per CTA (16-bit Q; same-type cache at
 // d = 64 or 128, or an fp8 E5M2 cache at d = 128)
 constexpr int PF_BM_TC2 = 256;

@@ -1,5 +1,6 @@
 // Varlen causal paged prefill on the tcgen05 tensor cores (sm_103a), head
-// dim 256.
+// dim 256: `prefill_tc_kernel` for 16-bit caches, `prefill_tc8_kernel` (at
+// the end of the file) for fp8 E5M2 caches widened in shared memory.
 //
 // Computes the same attention as every other path of the library (the
 // packed-varlen interface with one block table per row and bottom-right
@@ -498,6 +499,508 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// fp8 E5M2 caches at d = 256: the same layout with the codes streamed by TMA
+// into their own rings and widened by two warps into the 16-bit tiles the
+// MMAs read (an E5M2 code is the high byte of the binary16 of the same value;
+// for bf16 Q it is widened through fp32, also exactly).  Shared memory:
+// 16-bit K 64 KB (one tile), 16-bit V 2 x 32 KB (the two halves of a tile),
+// K codes 2 x 32 KB, V codes 2 x 16 KB, and the 1 KB through which the two
+// softmax warpgroups swap partial row maxima and sums.
+struct Tc8Cfg {
+  static constexpr int D = 256;
+  static constexpr int BM = 128;                      // query rows per CTA = TMEM lanes
+  static constexpr int BN = 128;                      // keys per S tile
+  static constexpr int HB = 64;                       // keys per V half
+  static constexpr int NC8 = D / 128;                 // 128-byte chunks of a code row
+  static constexpr uint32_t K_BYTES = BN * D * 2;     // 16-bit K: [chunk][128 keys][128 B]
+  static constexpr uint32_t V_BYTES = HB * D * 2;     // 16-bit V half: [chunk][64 keys][128 B]
+  static constexpr uint32_t K8_BYTES = BN * D;        // K codes: [chunk][128 keys][128 B]
+  static constexpr uint32_t V8_BYTES = HB * D;        // V codes: [chunk][64 keys][128 B]
+  static constexpr int S8 = 2;                        // code stages (K and V each)
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + K_BYTES;
+  static constexpr uint32_t OFF_K8 = OFF_V + 2 * V_BYTES;
+  static constexpr uint32_t OFF_V8 = OFF_K8 + S8 * K8_BYTES;
+  static constexpr uint32_t OFF_X = OFF_V8 + S8 * V8_BYTES;  // [2][128] floats: partial maxima / sums
+  static constexpr uint32_t OFF_BAR = OFF_X + 2 * BM * 4;
+  static constexpr uint32_t BAR_AREA = 192;           // mbarriers, then TMEM address and flags
+  static constexpr uint32_t SMEM = OFF_BAR + BAR_AREA + 16 + 1024;  // alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t O_COL = BN;               // S in [0, BN), P over its first BN / 2
+  static constexpr uint32_t Q_COL = O_COL + D;
+  // barrier indices
+  static constexpr int B_KF = 0,                      // 16-bit K tile widened (2 warps)
+      B_KE = B_KF + 1,                                // S(j) done with it
+      B_VF = B_KE + 1,                                // [2] 16-bit V half h widened (2 warps)
+      B_VE = B_VF + 2,                                // [2] P V half h done with it
+      B_SF = B_VE + 2,                                // S(j) written
+      B_PF = B_SF + 1,                                // P(j) written (8 warps)
+      B_PV = B_PF + 1,                                // O += P(j) V done
+      B_Q = B_PV + 1,                                 // Q in TMEM (8 warps)
+      B_DRAIN = B_Q + 1,
+      B_K8F = B_DRAIN + 1, B_K8E = B_K8F + S8,        // code rings: full (TMA) / empty (2 warps)
+      B_V8F = B_K8E + S8, B_V8E = B_V8F + S8, NBAR = B_V8E + S8;
+  static_assert(Q_COL + D / 2 == TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
+};
+
+template <typename T>
+__global__ void __launch_bounds__(384, 1)
+    prefill_tc8_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV) {
+  using C = Tc8Cfg;
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V;
+  const uint32_t sK8 = base + C::OFF_K8, sV8 = base + C::OFF_V8;
+  volatile float* xch = reinterpret_cast<volatile float*>(smem + C::OFF_X);
+  const uint32_t bar0 = base + C::OFF_BAR;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::BAR_AREA);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::BAR_AREA + 4);
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+
+  const Problem& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work item (uniform over the CTA) -----------------------------------
+  // 1-D grid, KV head slowest: CTAs that run together read the same heads'
+  // K/V (L2 reuse); within a head the work list is longest-first
+  const int n_items = (int)(gridDim.x / p.hkv);
+  const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
+  if (item >= (int)*a.n_tiles) return;
+  const int2 wi = a.tiles[item];
+  const int b = wi.x, mb = wi.y & 0xFFFFFF, part = wi.y >> 24;
+  const int qs = __ldg(p.cu_q + b);
+  const int qb = __ldg(p.cu_q + b + 1) - qs;
+  const int L = __ldg(p.seq_lens + b);
+  if (qb <= 0) return;
+  if (qs < 0 || qs + qb > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    return;
+  }
+  const int g = p.g, M = qb * g, R0 = mb * C::BM;
+  if (R0 >= M) return;
+  const int r_last = min(R0 + C::BM, M) - 1;
+  const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
+  // the item's key range [k0, k1): the whole range, or one part of it
+  int per_u;
+  const bool cut = pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per_u) > 1;
+  const int k0 = cut ? part * per_u * PF_UNIT : 0;
+  const int k1 = cut ? min(k_end, (part + 1) * per_u * PF_UNIT) : k_end;
+  const int n_tiles = k1 > k0 ? (k1 - k0 + C::BN - 1) / C::BN : 0;
+
+  // ---- barriers and TMEM ----------------------------------------------------
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KF), 2);
+    mbar_init(bar(C::B_KE), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_VF + s), 2);
+      mbar_init(bar(C::B_VE + s), 1);
+    }
+    mbar_init(bar(C::B_SF), 1);
+    mbar_init(bar(C::B_PF), 8);
+    mbar_init(bar(C::B_PV), 1);
+    mbar_init(bar(C::B_Q), 8);
+    mbar_init(bar(C::B_DRAIN), 1);
+    for (int s = 0; s < C::S8; ++s) {
+      mbar_init(bar(C::B_K8F + s), 1);
+      mbar_init(bar(C::B_K8E + s), 2);
+      mbar_init(bar(C::B_V8F + s), 1);
+      mbar_init(bar(C::B_V8E + s), 2);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ===== warp 0 streams the codes of each key tile: K (128 keys), then V ==
+    // in two 64-key halves, into the code rings: one TMA box (16 keys x 128
+    // codes) per page slot and 128-code chunk of the row; the slot holding
+    // the row's last key is copied by hand, zero-filled past the row's end.
+    const uint8_t* kc8 = static_cast<const uint8_t*>(a.kc);
+    const uint8_t* vc8 = static_cast<const uint8_t*>(a.vc);
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int P = p.page_size;
+    const int64_t bt_row = (int64_t)b * p.max_pages;
+    // `rows` keys from kbase into the [chunk][rows][128 B] code tile dst
+    auto unit = [&](const void* tmap, const uint8_t* cache, int kbase, int rows, uint32_t dst,
+                    uint32_t fb) {
+      // slot `lane`: 1 = whole slot by TMA, 2 = partial (by hand), 3 = zero-fill
+      int kind = 0, tok0 = 0;
+      if (lane < rows / 16) {
+        const int s0 = kbase + 16 * lane;
+        if (s0 >= L) {
+          kind = 3;
+        } else {
+          const int col = s0 / P;
+          const int page = col < p.max_pages ? __ldg(p.bt + bt_row + col) : -1;
+          if (page < 0 || page >= p.num_pages) {
+            atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+            kind = 3;
+          } else {
+            tok0 = page * P + (s0 % P);
+            kind = (s0 + 16 <= L) ? 1 : 2;
+          }
+        }
+      }
+      uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
+      while (manual) {
+        const int s = __ffs(manual) - 1;
+        manual &= manual - 1;
+        const int ks = __shfl_sync(0xffffffffu, kind, s);
+        const int t0 = __shfl_sync(0xffffffffu, tok0, s);
+        const int nvalid = ks == 2 ? L - (kbase + 16 * s) : 0;
+        for (int it = lane; it < 16 * (D / 16); it += 32) {
+          const int u16 = it % (D / 16), rr = it / (D / 16);  // 16-code unit of key row rr
+          const int c8 = u16 >> 3, pu = u16 & 7;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (rr < nvalid)
+            v = __ldg(reinterpret_cast<const uint4*>(cache + ((int64_t)(t0 + rr) * p.hkv + kh) * D +
+                                                     u16 * 16));
+          const int row = 16 * s + rr;
+          st_shared_v4(dst + c8 * (rows * 128) + row * 128 + ((pu ^ (row & 7)) << 4), v);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
+      if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_tma * 16u * (uint32_t)D);
+      __syncwarp();
+      if (kind == 1) {
+#pragma unroll
+        for (int c8 = 0; c8 < C::NC8; ++c8)
+          tma_load_3d(dst + c8 * (rows * 128) + lane * 16 * 128, tmap, c8 * 128, kh, tok0, fb);
+      }
+    };
+    bool ok = true;
+    int nk = 0, nv = 0;  // K / V code units started
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (j >= C::S8) ok = mbar_wait(bar(C::B_K8E + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      unit(&tmK, kc8, k0 + j * C::BN, C::BN, sK8 + (j & 1) * C::K8_BYTES, bar(C::B_K8F + (j & 1)));
+      ++nk;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = 2 * j + h;
+        if (q >= C::S8) ok = mbar_wait(bar(C::B_V8E + (q & 1)), ((q >> 1) - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        unit(&tmV, vc8, k0 + q * C::HB, C::HB, sV8 + (q & 1) * C::V8_BYTES, bar(C::B_V8F + (q & 1)));
+        ++nv;
+      }
+    }
+    if (!ok) {
+      // copies this warp started may still be landing: wait for them
+      for (int u = max(0, nk - C::S8); u < nk; ++u)
+        mbar_drain(bar(C::B_K8F + (u & 1)), (u >> 1) & 1, p.err);
+      for (int u = max(0, nv - C::S8); u < nv; ++u)
+        mbar_drain(bar(C::B_V8F + (u & 1)), (u >> 1) & 1, p.err);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ===== warps 2 and 3 widen every K tile (64 keys each) and V half (32 ===
+    // keys each) into the 16-bit tiles; lane = 16 codes of one key per step
+    const int ww = warp - 2;
+    const int u8 = lane & 7, c = u8 >> 2, va = 2 * (u8 & 3);
+    auto widen = [&](uint32_t src, uint32_t dst, int rows, int key0, int nkeys) {
+#pragma unroll
+      for (int c8 = 0; c8 < C::NC8; ++c8) {
+#pragma unroll 4
+        for (int it = 0; it < nkeys / 4; ++it) {
+          const int key = key0 + 4 * it + (lane >> 3);
+          const uint4 w = ld_shared_v4(src + c8 * (rows * 128) + key * 128 + ((u8 ^ (key & 7)) << 4));
+          uint4 lo, hi;
+          e5m2x4_to<T>(w.x, lo.x, lo.y);
+          e5m2x4_to<T>(w.y, lo.z, lo.w);
+          e5m2x4_to<T>(w.z, hi.x, hi.y);
+          e5m2x4_to<T>(w.w, hi.z, hi.w);
+          const uint32_t row = dst + (2 * c8 + c) * (rows * 128) + key * 128;
+          st_shared_v4(row + ((va ^ (key & 7)) << 4), lo);
+          st_shared_v4(row + (((va + 1) ^ (key & 7)) << 4), hi);
+        }
+      }
+      // the MMAs read the tile through the async proxy; TMA overwrites the
+      // codes next
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      ok = mbar_wait(bar(C::B_K8F + (j & 1)), (j >> 1) & 1, abort_flag, p.err);
+      if (ok && j >= 1) ok = mbar_wait(bar(C::B_KE), (j - 1) & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      widen(sK8 + (j & 1) * C::K8_BYTES, sK, C::BN, 64 * ww, 64);
+      if (lane == 0) {
+        mbar_arrive(bar(C::B_KF));
+        mbar_arrive(bar(C::B_K8E + (j & 1)));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int q = 2 * j + h;
+        ok = mbar_wait(bar(C::B_V8F + (q & 1)), (q >> 1) & 1, abort_flag, p.err);
+        if (ok && j >= 1) ok = mbar_wait(bar(C::B_VE + h), (j - 1) & 1, abort_flag, p.err);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        widen(sV8 + (q & 1) * C::V8_BYTES, sV + h * C::V_BYTES, C::HB, 32 * ww, 32);
+        if (lane == 0) {
+          mbar_arrive(bar(C::B_VF + h));
+          mbar_arrive(bar(C::B_V8E + (q & 1)));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (one thread) =======================
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+      constexpr uint32_t idS = idesc_f16(fmt, 128, C::BN, false);
+      constexpr uint32_t idO = idesc_f16(fmt, 128, D, true);
+      bool ok = n_tiles == 0 || mbar_wait(bar(C::B_Q), 0, abort_flag, p.err);
+      if (ok) tc_fence_after();
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        // S(j) = Q K(j)^T: A = Q from TMEM; it overwrites P(j-1), so the
+        // previous P V product must be done
+        ok = mbar_wait(bar(C::B_KF), j & 1, abort_flag, p.err);
+        if (ok && j >= 1) ok = mbar_wait(bar(C::B_PV), (j - 1) & 1, abort_flag, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t b0 = sdesc_sw128(sK, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t bd = b0 + (uint64_t)(((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4);
+          tc_mma_f16_ts(tmem, tmem + C::Q_COL + 8 * k, bd, idS, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(C::B_SF));
+        tc_commit(bar(C::B_KE));
+        // O += P(j) V(j), V in two halves of HB keys
+        ok = mbar_wait(bar(C::B_PF), j & 1, abort_flag, p.err);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (ok) ok = mbar_wait(bar(C::B_VF + h), j & 1, abort_flag, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t v0 = sdesc_sw128(sV + h * C::V_BYTES, C::HB * 128, 1024);
+#pragma unroll
+          for (int k = 0; k < C::HB / 16; ++k) {
+            // A = P from TMEM: 16 keys = 8 columns of 16-bit pairs
+            const uint64_t bd = v0 + (uint64_t)((k * 16 * 128) >> 4);
+            tc_mma_f16_ts(tmem + C::O_COL, tmem + (h * (C::HB / 16) + k) * 8, bd, idO,
+                          (j > 0 || h > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_VE + h));
+        }
+        if (!ok) break;
+        tc_commit(bar(C::B_PV));
+      }
+      // nothing this thread issued may still run once TMEM is freed
+      tc_commit(bar(C::B_DRAIN));
+      mbar_drain(bar(C::B_DRAIN), 0, p.err);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============ Q, softmax, epilogue =========================================
+    // Warpgroup hf (warps 4-7: hf = 0, warps 8-11: hf = 1) owns key columns
+    // [hf BN/2, (hf+1) BN/2) of each S tile and head-dim columns [hf d/2,
+    // (hf+1) d/2) of Q and of O.  The loop never leaves early: after a
+    // timed-out wait it runs on (flag raised, waits return at once), so both
+    // warpgroups always meet the same barriers.
+    constexpr int HN = C::BN / 2, HD = D / 2;
+    const int hf = warp >= 8 ? 1 : 0;
+    const int q4 = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = q4 * 32 + lane;     // tile row == TMEM lane
+    const int R = R0 + r;
+    const bool valid = R < M;
+    const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
+    const int last = valid ? L - qb + i - k0 : -1 - k0;  // last visible key, from k0
+    const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
+    const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
+    {
+      // this warpgroup's half of the row's Q into TMEM (16-bit pairs)
+      const T* qrow = static_cast<const T*>(a.q) + qoff + hf * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t v[32];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint4 u = valid ? __ldg(reinterpret_cast<const uint4*>(qrow + c * 64 + w * 8))
+                                : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * w] = u.x;
+          v[4 * w + 1] = u.y;
+          v[4 * w + 2] = u.z;
+          v[4 * w + 3] = u.w;
+        }
+        tmem_st_x32(trow + C::Q_COL + hf * (HD / 2) + c * 32, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_Q));
+    }
+    const float sl2 = p.sl2;
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < n_tiles; ++j) {
+      mbar_wait(bar(C::B_SF), j & 1, abort_flag, p.err);
+      tc_fence_after();
+      // S(j) was issued after the previous P V product completed: O is stable
+      float x[HN];
+      float mt;  // max raw logit of this half tile (masked keys -> -inf)
+      {
+        uint32_t u[HN];
+        mt = tmem_ld_red_max_x64(trow + hf * HN, u);  // the load also returns the max
+#pragma unroll
+        for (int k = 0; k < HN; ++k) x[k] = __uint_as_float(u[k]);
+      }
+      const int kb = j * C::BN + hf * HN;
+      if (kb + HN - 1 > last) {
+#pragma unroll
+        for (int k = 0; k < HN; ++k)
+          if (kb + k > last) x[k] = -INFINITY;
+        float pm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+#pragma unroll
+        for (int k = 8; k < HN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      }
+      {
+        // swap partial maxima through shared memory (the next tile's write
+        // comes after S(j + 1), which waits for this tile's P V product,
+        // which waits for both warpgroups' P, published after these reads)
+        xch[hf * C::BM + r] = mt;
+        named_bar_sync(1, 256);
+        mt = fmaxf(mt, xch[(hf ^ 1) * C::BM + r]);
+      }
+      const float m_new = fmaxf(m_used, mt * sl2);  // sl2 > 0: max commutes with the scale
+      float factor = 1.f;
+      bool need = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + 8.f) {
+        need = true;
+        factor = ex2(m_used - m_new);
+        m_used = m_new;
+      }
+      const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+          tmem_st_x32(trow + C::O_COL + hf * HD + c * 32, o);
+        }
+      }
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+#pragma unroll
+      for (int k = 0; k < HN; ++k) {
+        x[k] = ex2(fmaf(x[k], sl2, nmu));
+        ps[k & 7] += x[k];
+      }
+      {
+        // P (16-bit pairs) over this warpgroup's keys: HN / 2 columns at the
+        // start of S, then one arrival per warp
+        uint32_t pk[HN / 2];
+#pragma unroll
+        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
+        tmem_st_x32(trow + hf * (HN / 2), pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PF));
+      }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l = l * factor + rs;
+    }
+    // ---- epilogue: out = O / (l_0 + l_1) * v_scale, or this part's state ----
+    if (n_tiles > 0) {
+      mbar_wait(bar(C::B_PV), (n_tiles - 1) & 1, abort_flag, p.err);
+      tc_fence_after();
+    }
+    // the partial row sums, swapped through shared memory once every read
+    // of the maxima is done, added in warpgroup order
+    named_bar_sync(1, 256);
+    xch[hf * C::BM + r] = l;
+    named_bar_sync(1, 256);
+    const float lo = xch[(hf ^ 1) * C::BM + r];
+    const float lt = hf == 0 ? l + lo : lo + l;
+    T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
+    if (cut) {
+      // this part's unnormalised O (each warpgroup its d / 2 columns), the
+      // maximum it is relative to and the row sum, for the merge
+      const int64_t slot = ((int64_t)(qs + i) * p.hq + kh * g + hg) * a.pf_parts + part;
+      if (valid && hf == 0)
+        a.pf_ml[slot] = make_float2(n_tiles > 0 ? m_used : -INFINITY, n_tiles > 0 ? lt : 0.f);
+      float* prow = a.pf_acc + slot * D + hf * HD;
+      if (n_tiles > 0) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              *reinterpret_cast<uint4*>(prow + c * 32 + 4 * w) =
+                  make_uint4(o[4 * w], o[4 * w + 1], o[4 * w + 2], o[4 * w + 3]);
+          }
+        }
+      }
+    } else if (n_tiles > 0) {
+      const float inv = lt > 0.f ? p.v_scale / lt : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld_x32(trow + C::O_COL + hf * HD + c * 32, o);
+        if (valid) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 v;
+            v.x = pack2<T>(__uint_as_float(o[8 * w + 0]) * inv, __uint_as_float(o[8 * w + 1]) * inv);
+            v.y = pack2<T>(__uint_as_float(o[8 * w + 2]) * inv, __uint_as_float(o[8 * w + 3]) * inv);
+            v.z = pack2<T>(__uint_as_float(o[8 * w + 4]) * inv, __uint_as_float(o[8 * w + 5]) * inv);
+            v.w = pack2<T>(__uint_as_float(o[8 * w + 6]) * inv, __uint_as_float(o[8 * w + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * w) = v;
+          }
+        }
+      }
+    } else if (valid) {
+      // no key visible to any row of the tile
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c)
+        *reinterpret_cast<uint4*>(orow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -540,34 +1043,37 @@ namespace {
 
 template <typename T>
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
-                      cudaStream_t st) {
-  auto k = prefill_tc_kernel<T>;
-  static DeviceFlags attr;
-  cudaError_t e = attr.once([&] {
-    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
+                      bool kv8, cudaStream_t st) {
+  auto k = kv8 ? prefill_tc8_kernel<T> : prefill_tc_kernel<T>;
+  const uint32_t smem = kv8 ? Tc8Cfg::SMEM : TcCfg::SMEM;
+  static DeviceFlags attr16, attr8;
+  cudaError_t e = (kv8 ? attr8 : attr16).once([&] {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, TcCfg::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
-  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && kv_dtype == q_dtype && d == 256 &&
-         cache_tokens < (int64_t(1) << 31) && encode_fn() != nullptr;
+  return (q_dtype == PA_BF16 || q_dtype == PA_F16) && (kv_dtype == q_dtype || kv_dtype == PA_E5M2) &&
+         d == 256 && cache_tokens < (int64_t(1) << 31) && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int kv_dtype, int grid_x,
+                              cudaStream_t st) {
   if (grid_x == 0) return cudaSuccess;
   if (a.p.d != 256) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;
-  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+  if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
-  return q_dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, tk, tv, grid_x, st)
-                            : launch_tc<__half>(a, tk, tv, grid_x, st);
+  const bool kv8 = kv_dtype == PA_E5M2;
+  return q_dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, tk, tv, grid_x, kv8, st)
+                            : launch_tc<__half>(a, tk, tv, grid_x, kv8, st);
 }
 
 }  // namespace pa

@@ -81,7 +81,8 @@ def bitwise(a, b):
 @pytest.mark.parametrize("dtype,kv,d", [("bf16", None, 128), ("f16", None, 128),
                                         ("bf16", None, 64), ("f16", None, 256),
                                         ("bf16", None, 256), ("f16", "e5m2", 128),
-                                        ("bf16", "e5m2", 128)])
+                                        ("bf16", "e5m2", 128), ("f16", "e5m2", 256),
+                                        ("bf16", "e5m2", 256)])
 def test_cut_items_match_oracle(dtype, kv, d):
     cpu, gpu = batch(d=d, dtype=dtype, kv=kv, seed=31 + d)
     tol = TOL["e5m2" if kv else dtype]
@@ -98,7 +99,7 @@ def test_cut_items_match_oracle(dtype, kv, d):
     assert bitwise(cut[365:465], whole[365:465]) and bitwise(cut[465:], whole[465:])
 
 
-@pytest.mark.parametrize("dtype,kv,d", [("f32", None, 128), ("f16", "e5m2", 256),
+@pytest.mark.parametrize("dtype,kv,d", [("f32", None, 128), ("f16", "e5m2", 64),
                                         ("bf16", "e5m2", 64)])
 def test_paths_that_do_not_cut_ignore_the_field(dtype, kv, d):
     ql, kl = [40, 3], [17000, 17000]
