@@ -611,8 +611,11 @@ def run_profile(args):
     import paged_kv_attention_prefill_gb300 as pa
     from paged_kv_attention_prefill_gb300 import build as pa_build
     pa_build.build()
-    n = {"prefill": 2, "mixed3": 3, "decode4": 4, "decode5": 5, "decode1": 1}[args.profile]
-    full = workloads.make_workload(n, device="cuda", data_device="cuda")
+    n = {"prefill": 2, "mixed3": 3, "mixed3fp8": 3, "decode4": 4, "decode5": 5,
+         "decode1": 1}[args.profile]
+    # mixed3fp8: the mixed workload with fp16 Q and an fp8 E5M2 cache
+    over = dict(kv_dtype="e5m2", k_scale=0.5, v_scale=2.0) if args.profile == "mixed3fp8" else {}
+    full = workloads.make_workload(n, device="cuda", data_device="cuda", **over)
     b = full if not args.profile_rows else workloads.sub_batch(
         full, list(range(min(args.profile_rows, full.num_rows))), device="cuda")
     del full
@@ -637,7 +640,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
-    ap.add_argument("--profile", choices=["prefill", "mixed3", "decode4", "decode5", "decode1"])
+    ap.add_argument("--profile", choices=["prefill", "mixed3", "mixed3fp8", "decode4", "decode5",
+                                          "decode1"])
     ap.add_argument("--profile-rows", type=int, default=0)
     args = ap.parse_args()
     if args.profile:
