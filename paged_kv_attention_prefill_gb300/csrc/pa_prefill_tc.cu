@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // fp8 E5M2 caches at d = 256: the same layout with the codes streamed by TMA
-// into their own rings and widened by two warps into the 16-bit tiles the
-// MMAs read (an E5M2 code is the high byte of the binary16 of the same value;
+// into their own rings and widened by four more warps (12-15; warps 2 and 3
+// idle) into the 16-bit tiles the MMAs read (an E5M2 code is the high byte of the binary16 of the same value;
 // for bf16 Q it is widened through fp32, also exactly).  Shared memory:
 // 16-bit K 64 KB (one tile), 16-bit V 2 x 32 KB (the two halves of a tile),
 // K codes 2 x 32 KB, V codes 2 x 16 KB, and the 1 KB through which the two
@@ -517,6 +517,8 @@ struct Tc8Cfg {
   static constexpr uint32_t K8_BYTES = BN * D;        // K codes: [chunk][128 keys][128 B]
   static constexpr uint32_t V8_BYTES = HB * D;        // V codes: [chunk][64 keys][128 B]
   static constexpr int S8 = 2;                        // code stages (K and V each)
+  static constexpr int NW = 4;                        // widening warps (12-15)
+  static constexpr int THREADS = 512;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + K_BYTES;
   static constexpr uint32_t OFF_K8 = OFF_V + 2 * V_BYTES;
@@ -529,16 +531,16 @@ struct Tc8Cfg {
   static constexpr uint32_t O_COL = BN;               // S in [0, BN), P over its first BN / 2
   static constexpr uint32_t Q_COL = O_COL + D;
   // barrier indices
-  static constexpr int B_KF = 0,                      // 16-bit K tile widened (2 warps)
+  static constexpr int B_KF = 0,                      // 16-bit K tile widened (NW warps)
       B_KE = B_KF + 1,                                // S(j) done with it
-      B_VF = B_KE + 1,                                // [2] 16-bit V half h widened (2 warps)
+      B_VF = B_KE + 1,                                // [2] 16-bit V half h widened (NW warps)
       B_VE = B_VF + 2,                                // [2] P V half h done with it
       B_SF = B_VE + 2,                                // S(j) written
       B_PF = B_SF + 1,                                // P(j) written (8 warps)
       B_PV = B_PF + 1,                                // O += P(j) V done
       B_Q = B_PV + 1,                                 // Q in TMEM (8 warps)
       B_DRAIN = B_Q + 1,
-      B_K8F = B_DRAIN + 1, B_K8E = B_K8F + S8,        // code rings: full (TMA) / empty (2 warps)
+      B_K8F = B_DRAIN + 1, B_K8E = B_K8F + S8,        // code rings: full (TMA) / empty (NW warps)
       B_V8F = B_K8E + S8, B_V8E = B_V8F + S8, NBAR = B_V8E + S8;
   static_assert(Q_COL + D / 2 == TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -546,7 +548,7 @@ struct Tc8Cfg {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
     prefill_tc8_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using C = Tc8Cfg;
@@ -595,10 +597,10 @@ __global__ void __launch_bounds__(384, 1)
 
   // ---- barriers and TMEM ----------------------------------------------------
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::B_KF), 2);
+    mbar_init(bar(C::B_KF), C::NW);
     mbar_init(bar(C::B_KE), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::B_VF + s), 2);
+      mbar_init(bar(C::B_VF + s), C::NW);
       mbar_init(bar(C::B_VE + s), 1);
     }
     mbar_init(bar(C::B_SF), 1);
@@ -608,9 +610,9 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::B_DRAIN), 1);
     for (int s = 0; s < C::S8; ++s) {
       mbar_init(bar(C::B_K8F + s), 1);
-      mbar_init(bar(C::B_K8E + s), 2);
+      mbar_init(bar(C::B_K8E + s), C::NW);
       mbar_init(bar(C::B_V8F + s), 1);
-      mbar_init(bar(C::B_V8E + s), 2);
+      mbar_init(bar(C::B_V8E + s), C::NW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -716,10 +718,10 @@ __global__ void __launch_bounds__(384, 1)
       for (int u = max(0, nv - C::S8); u < nv; ++u)
         mbar_drain(bar(C::B_V8F + (u & 1)), (u >> 1) & 1, p.err);
     }
-  } else if (warp == 2 || warp == 3) {
-    // ===== warps 2 and 3 widen every K tile (64 keys each) and V half (32 ===
+  } else if (warp >= 12) {
+    // ===== warps 12-15 widen every K tile (32 keys each) and V half (16 =====
     // keys each) into the 16-bit tiles; lane = 16 codes of one key per step
-    const int ww = warp - 2;
+    const int ww = warp - 12;
     const int u8 = lane & 7, c = u8 >> 2, va = 2 * (u8 & 3);
     auto widen = [&](uint32_t src, uint32_t dst, int rows, int key0, int nkeys) {
 #pragma unroll
@@ -751,7 +753,7 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
-      widen(sK8 + (j & 1) * C::K8_BYTES, sK, C::BN, 64 * ww, 64);
+      widen(sK8 + (j & 1) * C::K8_BYTES, sK, C::BN, (C::BN / C::NW) * ww, C::BN / C::NW);
       if (lane == 0) {
         mbar_arrive(bar(C::B_KF));
         mbar_arrive(bar(C::B_K8E + (j & 1)));
@@ -765,7 +767,8 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        widen(sV8 + (q & 1) * C::V8_BYTES, sV + h * C::V_BYTES, C::HB, 32 * ww, 32);
+        widen(sV8 + (q & 1) * C::V8_BYTES, sV + h * C::V_BYTES, C::HB, (C::HB / C::NW) * ww,
+              C::HB / C::NW);
         if (lane == 0) {
           mbar_arrive(bar(C::B_VF + h));
           mbar_arrive(bar(C::B_V8E + (q & 1)));
@@ -821,7 +824,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    // ============ Q, softmax, epilogue =========================================
+    // ============ Q, softmax, epilogue (warps 4-11) ============================
     // Warpgroup hf (warps 4-7: hf = 0, warps 8-11: hf = 1) owns key columns
     // [hf BN/2, (hf+1) BN/2) of each S tile and head-dim columns [hf d/2,
     // (hf+1) d/2) of Q and of O.  The loop never leaves early: after a
@@ -1051,7 +1054,7 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMa
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, smem, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), kv8 ? Tc8Cfg::THREADS : 384, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
