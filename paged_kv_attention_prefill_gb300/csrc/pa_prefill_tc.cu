@@ -499,13 +499,16 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// fp8 E5M2 caches at d = 256: the same layout with the codes streamed by TMA
-// into their own rings and widened by four more warps (12-15; warps 2 and 3
-// idle) into the 16-bit tiles the MMAs read (an E5M2 code is the high byte of the binary16 of the same value;
-// for bf16 Q it is widened through fp32, also exactly).  Shared memory:
-// 16-bit K 64 KB (one tile), 16-bit V 2 x 32 KB (the two halves of a tile),
-// K codes 2 x 32 KB, V codes 2 x 16 KB, and the 1 KB through which the two
-// softmax warpgroups swap partial row maxima and sums.
+// fp8 E5M2 caches at d = 256: Q in TMEM and 128-key S tiles as above, but P
+// stays over S in TMEM (its 32 KB of shared memory go to the code rings), so
+// S(j) waits for the previous P V product.  The codes are streamed by TMA
+// into their own rings and widened by a fourth warpgroup (warps 12-15;
+// warps 2 and 3 idle) into the 16-bit tiles the MMAs read: an E5M2 code is
+// the high byte of the binary16 of the same value, and for bf16 Q it is
+// widened through fp32, also exactly.  Shared memory: 16-bit K 64 KB (one
+// tile), 16-bit V 2 x 32 KB (the two halves of a tile), K codes 2 x 32 KB,
+// V codes 2 x 16 KB, and the 1 KB through which the two softmax warpgroups
+// swap partial row maxima and sums.
 struct Tc8Cfg {
   static constexpr int D = 256;
   static constexpr int BM = 128;                      // query rows per CTA = TMEM lanes
@@ -518,7 +521,7 @@ struct Tc8Cfg {
   static constexpr uint32_t V8_BYTES = HB * D;        // V codes: [chunk][64 keys][128 B]
   static constexpr int S8 = 2;                        // code stages (K and V each)
   static constexpr int NW = 4;                        // widening warps (12-15)
-  static constexpr int THREADS = 512;
+  static constexpr int THREADS = 512;                 // four warpgroups
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + K_BYTES;
   static constexpr uint32_t OFF_K8 = OFF_V + 2 * V_BYTES;
