@@ -46,8 +46,9 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # DRAM bytes (read + write) per launch of the prefill kernel on this workload,
-# from the ncu capture summarised in profiles/prefill_tc2_workload2.md.
-# Reported only while the kernel's sources are the ones that were profiled.
+# from one ncu capture of the headline step (dram__bytes_read.sum +
+# dram__bytes_write.sum of one prefill_tc2_kernel launch, page 16).  Reported
+# only while the kernel's sources hash to the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
         "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "83c1a930af3249858d381673482eb0e52f79bdc9d5646544c1e70a5f9ce38ad8",
@@ -164,6 +165,18 @@ def launches_per_call(q_lens, max_dq=16, mixed=True):
     if dec:
         n += 2 + (1 if n_rows >= 16 else 0)
     return n + (1 if pre else 0)
+
+
+def headline_config(b, world):
+    """The headline workload's description, the same for both arms."""
+    names = ("q", "k_cache", "v_cache", "block_table", "cu_seqlens_q", "seq_lens")
+    in_bytes = sum(getattr(b, k).numel() * getattr(b, k).element_size() for k in names)
+    return {"workload": workloads.WORKLOADS[HEADLINE_WORKLOAD], "rows": b.num_rows,
+            "q_lens": b.q_lens, "kv_lens": b.kv_lens, "page_size": b.page_size,
+            "flops_per_step": metrics.prefill_flops(b.q_lens, b.kv_lens, b.num_q_heads,
+                                                    b.head_dim),
+            "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush",
+            "parallelism": f"replicas x{world} (rows independent)"}
 
 
 def call_args(b):
@@ -544,11 +557,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16, shuffled block tables, poisoned unused slots)",
-            "config": {"workload": workloads.WORKLOADS[HEADLINE_WORKLOAD], "rows": b.num_rows,
-                       "q_lens": ql, "kv_lens": kl, "page_size": 16,
-                       "flops_per_step": F, "entry": "paged_attn_mixed",
-                       "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB > 129 MiB), no flush",
-                       "parallelism": f"replicas x{world} (rows independent)"},
+            "config": headline_config(b, world), "entry": "paged_attn_mixed",
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                          "peak": pk["bf16"], "unit": "TFLOP/s",
                          "frac": round(achieved / pk["bf16"], 4), "traffic": profiled_traffic(),
@@ -582,22 +591,27 @@ def run_reference(args):
     oracle.build()
     b = workloads.make_workload(HEADLINE_WORKLOAD, page_size=16)
     budget = max(0.5, args.ref_seconds)
-    vals, descr, cores = [], "", oracle.num_threads()
+    vals, secs, descr, cores = [], [], "", oracle.num_threads()
     for s in range(args.warmup + args.steps):
+        t = time.perf_counter()
         v, cores, descr, _ = cpu_baseline_sample(b, budget_s=budget, one_thread=False)
+        dt = time.perf_counter() - t
         if s >= args.warmup:
             vals.append(v)
+            secs.append(dt)
     value = statistics.median(vals)
     F = metrics.prefill_flops(b.q_lens, b.kv_lens, b.num_q_heads, b.head_dim)
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(F / (value * 1e12) * 1e3, 3) if value > 0 else None,
+           "ms_per_step": round(statistics.median(secs) * 1e3, 1),
+           "ms_per_step_note": "measured wall time of one step: one bounded sample of the "
+                               "workload's query tokens, not the whole workload",
+           "ms_whole_workload_extrapolated": round(F / (value * 1e12) * 1e3, 1) if value > 0 else None,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "config": {"workload": workloads.WORKLOADS[HEADLINE_WORKLOAD],
-                                            "page_size": 16, "flops_per_step": F},
+           "data": "synthetic (seeded N(0,1) bf16, shuffled block tables, poisoned unused slots)",
+           "config": headline_config(b, world), "entry": "oracle (fp64 C, OpenMP)",
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
-                            "kind": "oracle",
-                            "sample": f"per step: {descr}; ms_per_step extrapolates to the whole workload"},
+                            "kind": "oracle", "sample": f"per step: {descr}"},
            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
@@ -606,29 +620,35 @@ def run_reference(args):
 
 def run_profile(args):
     """Runs one part of the path `steps` times with no reporting: the command
-    that ncu captures.  --profile-rows keeps the first R rows of the
-    workload (a small case of the same kernel)."""
+    that ncu captures.  Only the profiled rows are generated on the device
+    (--profile-rows keeps the first R rows of the part; decode3 is the mixed
+    workload's three resident rows through the decode entry), so a capture
+    holds the small case it measures and nothing else."""
     import paged_kv_attention_prefill_gb300 as pa
     from paged_kv_attention_prefill_gb300 import build as pa_build
     pa_build.build()
-    n = {"prefill": 2, "mixed3": 3, "mixed3fp8": 3, "decode4": 4, "decode5": 5,
-         "decode1": 1}[args.profile]
+    n, rows = {"prefill": (2, None), "mixed3": (3, None), "mixed3fp8": (3, None),
+               "decode3": (3, [1, 2, 3]), "decode4": (4, None), "decode5": (5, None),
+               "decode1": (1, None)}[args.profile]
+    if rows is None:
+        rows = list(range(len(workloads.workload_lengths(n)[0])))
+    if args.profile_rows:
+        rows = rows[:args.profile_rows]
     # mixed3fp8: the mixed workload with fp16 Q and an fp8 E5M2 cache
     over = dict(kv_dtype="e5m2", k_scale=0.5, v_scale=2.0) if args.profile == "mixed3fp8" else {}
-    full = workloads.make_workload(n, device="cuda", data_device="cuda", **over)
-    b = full if not args.profile_rows else workloads.sub_batch(
-        full, list(range(min(args.profile_rows, full.num_rows))), device="cuda")
-    del full
+    b = workloads.make_workload(n, device="cuda", data_device="cuda", rows=rows, **over)
     torch.cuda.empty_cache()
-    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache, num_splits=args.num_splits),
+                           b.num_rows, b.total_q, "cuda")
     out = torch.empty_like(b.q)
     fn = pa.paged_attn_decode if args.profile.startswith("decode") else pa.paged_attn_mixed
     for _ in range(args.warmup + args.steps):
         fn(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens, out=out,
-           workspace=ws, **call_args(b))
+           workspace=ws, num_splits=args.num_splits, **call_args(b))
     torch.cuda.synchronize()
     print(f"profiled {args.profile}: rows={b.num_rows} total_q={b.total_q} "
-          f"cache={2 * b.k_cache.numel() * b.k_cache.element_size() / 2**20:.0f} MiB")
+          f"cache={2 * b.k_cache.numel() * b.k_cache.element_size() / 2**20:.0f} MiB "
+          f"device bytes held={torch.cuda.max_memory_allocated() / 2**20:.0f} MiB")
 
 
 def main():
@@ -640,8 +660,9 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=4.0)
-    ap.add_argument("--profile", choices=["prefill", "mixed3", "mixed3fp8", "decode4", "decode5",
-                                          "decode1"])
+    ap.add_argument("--profile", choices=["prefill", "mixed3", "mixed3fp8", "decode3", "decode4",
+                                          "decode5", "decode1"])
+    ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--profile-rows", type=int, default=0)
     args = ap.parse_args()
     if args.profile:

@@ -146,8 +146,8 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out=None,
           workspace=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-          verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0, cu_seqlens_q_host=None,
-          seq_lens_host=None, stream=None):
+          num_splits=0, verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0,
+          cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         if not t.is_cuda:
             raise PagedAttnError("all tensors must be CUDA tensors")
@@ -157,8 +157,8 @@ def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out
             seq_lens.dtype != torch.int32:
         raise PagedAttnError("block_table, cu_seqlens_q and seq_lens must be int32")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
-                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode,
-                      prefill_kv_parts=prefill_kv_parts)
+                      v_scale=v_scale, max_decode_q=max_decode_q, num_splits=num_splits,
+                      verify_mode=verify_mode, prefill_kv_parts=prefill_kv_parts)
     B = int(seq_lens.shape[0])
     total_q = int(q.shape[0])
     if out is None:

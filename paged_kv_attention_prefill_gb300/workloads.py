@@ -247,8 +247,15 @@ def workload_shape(n: int) -> dict:
 
 
 def make_workload(n: int, *, device="cpu", data_device=None, page_size: Optional[int] = None,
-                  perm_seed: Optional[int] = None, poison: str = "finite", **over) -> Batch:
+                  perm_seed: Optional[int] = None, poison: str = "finite",
+                  rows: Optional[Sequence[int]] = None, **over) -> Batch:
+    """Workload n.  ``rows`` keeps only the listed rows' lengths (the same
+    shapes and distributions; the data drawn for them differs from the whole
+    workload's), so a small case of the same kernels never holds the rest."""
     q_lens, kv_lens = workload_lengths(n)
+    if rows is not None:
+        q_lens = [q_lens[int(r)] for r in rows]
+        kv_lens = [kv_lens[int(r)] for r in rows]
     shape = workload_shape(n)
     if page_size is not None:
         shape["page_size"] = page_size

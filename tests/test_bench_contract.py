@@ -25,8 +25,16 @@ def test_reference_arm_prints_one_contract_line():
     assert d["n_gpus"] == 1 and d["steps"] == 1
     assert d["warmup"] >= 3  # the timing rules' floor, whatever was asked
     assert d["higher_is_better"] is True and d["scaling"] == "weak"
-    assert d["unit"] == "TFLOP/s" and d["data"] == "synthetic"
+    assert d["unit"] == "TFLOP/s" and d["data"].startswith("synthetic")
     assert isinstance(d["config"]["workload"], str) and d["config"]["flops_per_step"] > 0
+    # the GPU arm's config comes from the same function: same keys, same values
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_attention_prefill_gb300 import workloads
+    assert d["config"] == bench.headline_config(
+        workloads.make_workload(bench.HEADLINE_WORKLOAD, page_size=16), 1)
+    # ms_per_step is the measured time of one (sampled) step, not an extrapolation
+    assert d["ms_per_step"] < d["ms_whole_workload_extrapolated"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["unit"] == d["unit"] and cb["sample"]
