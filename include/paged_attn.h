@@ -121,7 +121,8 @@ typedef struct pa_params {
   int32_t max_decode_q;   /* mixed: rows with 1 <= q_b <= max_decode_q go to the
                              split-KV decode path; 0 selects 16.  decode: the
                              largest q_b allowed. */
-  int32_t num_splits;     /* split-KV parts per decode row: 0 or 16 */
+  int32_t num_splits;     /* split-KV parts per decode row: 0 or 16, or
+                             PA_SPLITS_BY_LENGTH, see below */
   int32_t verify_mode;    /* decode rows with q_b > 1: PA_VERIFY_PACKED (0) or
                              PA_VERIFY_TOKENWISE (1), see below */
   int32_t prefill_kv_parts; /* prefill work items cut into key-range parts:
@@ -181,6 +182,25 @@ enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
  */
 enum { PA_PREFILL_PARTS_AUTO = -1 };
 
+/*
+ * Length-only split count for long decode rows (num_splits =
+ * PA_SPLITS_BY_LENGTH).  vllm-rlt PR #128 ("Purpose", decode bullets) fixes
+ * the partition as a function of the row's own length -- what keeps a row's
+ * bits independent of the batch -- and its review thread leaves the count of
+ * 16 untuned.  In this mode a row of at most 32768 keys keeps the 16 parts of
+ * the default (bitwise the same result); a longer row is cut into parts of
+ * 2048 keys (whole 64-key tiles), at most 128 of them (longer parts past
+ * 262144 keys), and those parts run on the tcgen05 tile kernel with all of
+ * the row's q_b * g GQA-packed query rows in one 128-row tile, so each part's
+ * K/V is read once.  Still a function of the row's length alone: results
+ * stay batch-invariant, page-size- and page-order-independent.  The partial
+ * states take 128 slots per decode token and query head: the workspace is
+ * sized for that (8x the default's partial-state bytes).  Built for head_dim
+ * 256 with a 16-bit q and a same-type cache, packed verify rows; other
+ * combinations return PA_ERR_UNSUPPORTED from the decode and mixed calls.
+ */
+enum { PA_SPLITS_BY_LENGTH = -1 };
+
 typedef struct pa_batch {
   int32_t num_rows;             /* B >= 0 */
   int32_t total_q;              /* cu_seqlens_q[B], the rows of q and out */
@@ -209,6 +229,10 @@ typedef struct pa_batch {
 size_t paged_attn_workspace_size(const pa_params* params, int32_t num_rows, int32_t total_q);
 
 /*
+ * Defined by: vllm-rlt PR #128, "Purpose", prefill bullets (the packed varlen
+ * interface: cu_seqlens_q, one block table per sequence, bottom-right causal
+ * alignment, tiled online softmax over K/V gathered through the block table).
+ *
  * Varlen causal paged prefill: every row with q_b > 0, whatever its length,
  * on the prefill kernel (GQA-packed query tiles, online softmax over key
  * tiles, bottom-right causal mask).  Short rows are correct but slow here;
@@ -219,6 +243,10 @@ pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, con
                              void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Defined by: vllm-rlt PR #128, "Purpose", decode bullets (each row's keys cut
+ * into 16 equal, tile-aligned parts chosen from the row's length alone, fp32
+ * partial softmax states, a second kernel that merges them, a static grid).
+ *
  * Split-KV paged decode: every row (1 <= q_b <= max_decode_q; q_b > 1 are
  * speculative-verify rows) split into num_splits (16) contiguous parts of
  * whole 64-key tiles, chosen from L_b alone.  Each (row, KV head, split,
@@ -232,6 +260,10 @@ pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, cons
                             void* workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * Defined by: 1Cat-vLLM PR #616, original description, "Purpose" (decode and
+ * speculative-verify rows of a mixed batch sent to one paged decode launch
+ * instead of the per-sequence prefill loop).
+ *
  * Mixed serving batch: rows with 1 <= q_b <= max_decode_q go to the split-KV
  * decode path, longer rows to the prefill kernel, rows with q_b = 0 are
  * skipped.  The routing is computed on the device from cu_seqlens_q, so the
@@ -266,12 +298,14 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
  * paged_attn_decode with a workspace of your own for larger batches).  The
  * call never calls cudaMalloc, cudaFree or any allocating routine.
  *
- * The first call on a device does a one-time set-up (it looks up the array's
- * device address with that device current); make that first call before any
- * stream capture.  Every call shares the one array: calls whose work overlaps
- * on the GPU (different streams, or different host threads) race and may
- * corrupt each other's results -- serialize them.  Each call clears the
- * array's header; device-side error flags are not reported by this call.
+ * The first call on a device (and the first after its context was torn down
+ * and made again) does a one-time set-up: it looks up the array's device
+ * address with that device current; make that first call before any stream
+ * capture.  Every call shares the one array: calls whose work overlaps on the
+ * GPU (different streams, or different host threads) race and may corrupt
+ * each other's results -- serialize them.  Each call clears the array's work
+ * counters; its device-side error flags are sticky, like a workspace's, and
+ * paged_attn_read_errors(NULL, ...) reads and clears them.
  */
 #define PA_STATIC_SCRATCH_BYTES (16u << 20)
 pa_status paged_attn_decode_static(const pa_params* params, const pa_batch* batch, const void* q,
@@ -287,7 +321,9 @@ pa_status paged_attn_decode_static(const pa_params* params, const pa_batch* batc
 
 /*
  * Copies the workspace header's error flags to *flags (host) and clears
- * them.  Synchronizes `stream`.  Not a compute call.
+ * them.  workspace = NULL reads the flags of the array that
+ * paged_attn_decode_static uses on the current device.  Synchronizes
+ * `stream`.  Not a compute call.
  */
 pa_status paged_attn_read_errors(void* workspace, pa_stream_t stream, uint32_t* flags);
 

@@ -18,9 +18,14 @@ static int64_t max_tiles_for(int num_rows, int total_q, int g, int bm, int pf_pa
 }
 
 WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g,
-                          int pf_parts) {
+                          int pf_parts, int by_len) {
   WsLayout w{};
   w.max_slots = std::min<int64_t>(total_q, (int64_t)num_rows * max_decode_q);
+  w.split_stride = by_len ? NSPLIT_MAX : NSPLIT;
+  // long-row items: every row long, every split, every 128-row block
+  w.max_long = by_len ? (int64_t)num_rows * NSPLIT_MAX *
+                            (((int64_t)max_decode_q * g + LONG_BM - 1) / LONG_BM)
+                      : 0;
   // the smallest tile height in use
   w.max_tiles = max_tiles_for(num_rows, total_q, g, 16, pf_parts);
   size_t off = sizeof(WsHeader);
@@ -33,9 +38,11 @@ WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_deco
   w.tiles = off;
   off += align_up((size_t)w.max_tiles * 8, 256);
   w.part_ml = off;
-  off += align_up((size_t)w.max_slots * hq * NSPLIT * 8, 256);
+  off += align_up((size_t)w.max_slots * hq * w.split_stride * 8, 256);
   w.part_acc = off;
-  off += align_up((size_t)w.max_slots * hq * NSPLIT * d * 4, 256);
+  off += align_up((size_t)w.max_slots * hq * w.split_stride * d * 4, 256);
+  w.long_items = off;
+  off += align_up((size_t)w.max_long * 8, 256);
   const size_t pf = pf_parts > 1 ? (size_t)total_q * hq * pf_parts : 0;
   w.pf_ml = off;
   off += align_up(pf * 8, 256);
@@ -46,6 +53,9 @@ WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_deco
 }
 
 namespace {
+
+// The device address of the array paged_attn_decode_static uses (end of file).
+pa_status static_scratch_address(void** out);
 
 struct Resolved {
   int hq, hkv, g, d, P;
@@ -64,6 +74,10 @@ struct Resolved {
   bool pf_auto;       // part count chosen per call
   int pf_cut;         // key-range parts in use (the tcgen05 kernels cut; others do not)
   int pf_min_units;   // least 128-key units per part
+  int by_len;         // length-only split count for long decode rows
+  bool long_tc;       // long decode rows on the tcgen05 kernel
+  int host_long;      // long-row decode work items (host mirrors)
+  int host_short;     // decode rows on the decode kernel (host mirrors)
 };
 
 // 0 = not checked, 1 = sm_103, 2 = other
@@ -97,7 +111,10 @@ pa_status resolve_params(const pa_params* prm, Resolved* r) {
   const int qd = prm->q_dtype, kvd = prm->kv_dtype;
   if (qd != PA_BF16 && qd != PA_F16 && qd != PA_F32) return PA_ERR_UNSUPPORTED;
   if (!(kvd == qd || (kvd == PA_E5M2 && qd != PA_F32))) return PA_ERR_UNSUPPORTED;
-  if (prm->num_splits != 0 && prm->num_splits != NSPLIT) return PA_ERR_UNSUPPORTED;
+  if (prm->num_splits != 0 && prm->num_splits != NSPLIT &&
+      prm->num_splits != PA_SPLITS_BY_LENGTH)
+    return PA_ERR_UNSUPPORTED;
+  r->by_len = prm->num_splits == PA_SPLITS_BY_LENGTH;
   if (prm->max_decode_q < 0) return PA_ERR_INVALID_ARG;
   if (!(std::isfinite(prm->softmax_scale) && std::isfinite(prm->k_scale) &&
         std::isfinite(prm->v_scale)))
@@ -208,7 +225,8 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   if (bat->num_rows > 0 && (!kc || !vc)) return PA_ERR_INVALID_ARG;
   if ((int64_t)bat->total_q * r->g > INT32_MAX / 2) return PA_ERR_INVALID_ARG;
   const WsLayout w =
-      workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g, r->pf_parts);
+      workspace_layout(bat->num_rows, bat->total_q, r->hq, r->d, r->max_dq, r->g, r->pf_parts,
+                       r->by_len);
   if (ws_bytes < w.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
   const int64_t cache_tokens = (int64_t)bat->num_pages * r->P;
@@ -217,6 +235,16 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   // one-token verify rows run on the TMA decode kernel only
   if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
     return PA_ERR_UNSUPPORTED;
+  // length-only split counts for long rows: their splits run on the tcgen05
+  // tile kernel, built for d = 256 with 16-bit q and a same-type cache
+  r->long_tc = false;
+  if (r->by_len && entry != E_PREFILL) {
+    if (r->tokenwise || r->d != 256 || r->kvd != r->qd ||
+        !prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens) ||
+        !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
+      return PA_ERR_UNSUPPORTED;
+    r->long_tc = true;
+  }
   r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
   // an explicit part count applies as given; a count chosen per call needs
   // the host mirrors (below)
@@ -225,6 +253,8 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   r->host_max_q_dec = 0;
   r->host_tiles = 0;
   r->host_slots = 0;
+  r->host_long = 0;
+  r->host_short = 0;
   if (r->host) {
     const int32_t* cu = bat->cu_seqlens_q_host;
     const int32_t* lens = bat->seq_lens_host;
@@ -242,6 +272,10 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
       if (dec) {
         r->host_max_q_dec = std::max(r->host_max_q_dec, qb);
         r->host_slots += qb;
+        if (r->long_tc && qb >= 1 && dec_is_long(L, 1))
+          r->host_long += dec_num_splits(L, 1) * ((qb * r->g + LONG_BM - 1) / LONG_BM);
+        else if (qb >= 1)
+          ++r->host_short;
       } else if (qb > 0) {
         const int nmb = (qb * r->g + bm - 1) / bm;
         for (int m = 0; m < nmb; ++m) {
@@ -270,7 +304,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
 AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const void* kc,
                    const void* vc, void* out, void* ws) {
   const WsLayout w =
-      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts);
+      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts, r.by_len);
   uint8_t* base = static_cast<uint8_t*>(ws);
   AttnArgs a{};
   a.p.cu_q = bat->cu_seqlens_q;
@@ -307,12 +341,17 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.pf_min_units = r.pf_min_units;
   a.pf_ml = reinterpret_cast<float2*>(base + w.pf_ml);
   a.pf_acc = reinterpret_cast<float*>(base + w.pf_acc);
+  a.split_stride = w.split_stride;
+  a.by_len = r.long_tc ? 1 : 0;
+  a.long_items = reinterpret_cast<const int2*>(base + w.long_items);
+  a.n_long = &reinterpret_cast<const WsHeader*>(base)->n_long;
+  a.max_long = w.max_long;
   return a;
 }
 
 int32_t* row_order_of(void* ws, const pa_batch* bat, const Resolved& r) {
   const WsLayout w =
-      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts);
+      workspace_layout(bat->num_rows, bat->total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts, r.by_len);
   return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + w.row_order);
 }
 
@@ -361,8 +400,19 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
                        int32_t* order, cudaStream_t st) {
   AttnArgs a = a0;
   a.dec_mblk = n_mblk;
-  cudaError_t e;
-  if (r.qd == PA_F32)
+  cudaError_t e = cudaSuccess;
+  if (r.long_tc && (!r.host || r.host_long > 0)) {
+    // rows longer than 32768 keys: the list of their (row, 128-row block,
+    // split) items, then those splits on the tcgen05 tile kernel
+    e = launch_long_items(a, const_cast<int2*>(a.long_items), a.max_long, st);
+    if (e != cudaSuccess) return e;
+    const int grid = r.host ? r.host_long * r.hkv : sm_count();
+    e = launch_decode_long(a, r.qd, grid, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (r.long_tc && r.host && r.host_short == 0) {
+    // every decode row was long: nothing for the decode kernel
+  } else if (r.qd == PA_F32)
     e = launch_f32(a, 1, 0, n_mblk, st);
   else if (decode_tma_supported(r.qd, r.kvd, r.d, (int64_t)a.p.num_pages * a.p.page_size)) {
     if (!r.tokenwise && order && a.p.num_rows >= ORDER_MIN_ROWS &&
@@ -407,7 +457,7 @@ extern "C" {
 size_t paged_attn_workspace_size(const pa_params* params, int32_t num_rows, int32_t total_q) {
   Resolved r;
   if (resolve_params(params, &r) != PA_OK || num_rows < 0 || total_q < 0) return 0;
-  return workspace_layout(num_rows, total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts).total;
+  return workspace_layout(num_rows, total_q, r.hq, r.d, r.max_dq, r.g, r.pf_parts, r.by_len).total;
 }
 
 pa_status paged_attn_prefill(const pa_params* params, const pa_batch* batch, const void* q,
@@ -456,7 +506,7 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, workspace);
   const WsLayout w = workspace_layout(batch->num_rows, batch->total_q, r.hq, r.d, r.max_dq, r.g,
-                                     r.pf_parts);
+                                     r.pf_parts, r.by_len);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   a.dec_base = reinterpret_cast<const int32_t*>(base + w.dec_base);
   a.slot_tok = reinterpret_cast<const int32_t*>(base + w.slot_tok);
@@ -497,7 +547,12 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
 }
 
 pa_status paged_attn_read_errors(void* workspace, pa_stream_t stream, uint32_t* flags) {
-  if (!workspace || !flags) return PA_ERR_INVALID_ARG;
+  if (!flags) return PA_ERR_INVALID_ARG;
+  if (!workspace) {
+    // the error word of the array paged_attn_decode_static uses
+    pa_status s = static_scratch_address(&workspace);
+    if (s != PA_OK) return s;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   if (cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -536,6 +591,8 @@ int32_t paged_attn_version(void) { return 100; }
 // file-scope device array: every GPU that loads the library holds it until
 // the process exits, and no call allocates or frees anything.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace pa {
@@ -543,23 +600,62 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_SCRATCH_BYTES];
 
-std::mutex g_static_mu;
-void* g_static_addr[64];  // the array's device address, per device
+// The current CUDA context's unique id (0 if none is current).  Looked up
+// through the driver entry points the runtime hands out, so the library links
+// no driver library.  Neither call allocates or touches a stream.
+unsigned long long current_context_id() {
+  using GetCur = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCur get_cur = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault,
+                                            &q) == cudaSuccess && q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetCur>(f) : nullptr;
+  }();
+  static GetId get_id = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                       cudaSuccess && q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<GetId>(f) : nullptr;
+  }();
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
-// One-time set-up per device (with that device current): look up where the
-// array lives.  The array's name is only a host-side stand-in in host code;
-// the kernels must be given this address.
+std::mutex g_static_mu;
+struct StaticAddr {
+  unsigned long long ctx = 0;  // context the address belongs to
+  void* addr = nullptr;
+};
+StaticAddr g_static_addr[64];  // per device
+
+// The array's device address in the current context (with that device
+// current).  In host code the array's name is only a host-side stand-in, so
+// the kernels must be given this address.  It is looked up once per context:
+// a context torn down and made again (cudaDeviceReset) gets a new id, and the
+// address is looked up afresh, since the module may then sit elsewhere.
 pa_status static_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_NO_DEVICE;
   if (dev < 0 || dev >= 64) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_addr[dev]) {
+  StaticAddr& e = g_static_addr[dev];
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || ctx != e.ctx || !e.addr) {
     void* p = nullptr;
+    // makes the device's primary context current if no context is yet
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-    g_static_addr[dev] = p;
+    const unsigned long long now = current_context_id();
+    if (now == 0) return PA_ERR_CUDA;
+    e.ctx = now;
+    e.addr = p;
   }
-  *out = g_static_addr[dev];
+  *out = e.addr;
   return PA_OK;
 }
 
@@ -582,9 +678,12 @@ extern "C" pa_status paged_attn_decode_static(const pa_params* params, const pa_
   s = static_scratch_address(&ws);
   if (s != PA_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents; the header (error word and
-  // the decode kernel's work counter) must start at zero
-  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), st) != cudaSuccess) return PA_ERR_CUDA;
+  // the array keeps the previous call's contents; the header's work counts
+  // and the decode kernel's work counter must start at zero.  The error word
+  // (the first 4 bytes) is left as it is: it is sticky, like a workspace's,
+  // and paged_attn_read_errors(NULL, ...) reads and clears it.
+  if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + 4, 0, sizeof(WsHeader) - 4, st) != cudaSuccess)
+    return PA_ERR_CUDA;
   AttnArgs a = make_args(r, batch, q, k_cache, v_cache, out, ws);
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
