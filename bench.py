@@ -264,6 +264,17 @@ def part_mixed3(steps, warmup, stream, pk):
     res = {"workload": workloads.WORKLOADS[3], "ms": round(ms, 4), "prefill_flops": F,
            "decode_bytes": byt, "whole_call_TFLOP/s_of_prefill": round(F / (ms * 1e-3) / 1e12, 1),
            "launches_per_call": launches_per_call(ql)}
+    lws = pa.make_workspace(pa.make_params(b.q, b.k_cache, num_splits=pa.PA_SPLITS_BY_LENGTH),
+                            b.num_rows, b.total_q, "cuda")
+
+    def lfn():
+        pa.paged_attn_mixed(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                            b.seq_lens, out=out, workspace=lws,
+                            num_splits=pa.PA_SPLITS_BY_LENGTH, **kw)
+    lms = time_calls(lfn, steps, warmup, stream)
+    res["whole_call_by_length"] = {"ms": round(lms, 4),
+                                   "TFLOP/s_of_prefill": round(F / (lms * 1e-3) / 1e12, 1)}
+    del lws
     # each half as a call of its own: the chunk's row through the prefill
     # entry, the three resident rows through the decode entry
     for name, rows, entry in (("prefill_row_alone", [0], pa.paged_attn_prefill),
@@ -285,6 +296,22 @@ def part_mixed3(steps, warmup, stream, pk):
             gbs = byt / (sms * 1e-3) / 1e9
             res[name] = {"ms": round(sms, 4), "GB/s": round(gbs, 1),
                          "frac_of_hbm": round(gbs / pk["hbm"], 4)}
+            # the same rows with the length-only split count for long rows
+            # (parts of 2048 keys on the tcgen05 tile kernel)
+            lws = pa.make_workspace(pa.make_params(sb.q, sb.k_cache,
+                                                   num_splits=pa.PA_SPLITS_BY_LENGTH),
+                                    sb.num_rows, sb.total_q, "cuda")
+
+            def lfn():
+                entry(sb.q, sb.k_cache, sb.v_cache, sb.block_table, sb.cu_seqlens_q, sb.seq_lens,
+                      out=sout, workspace=lws, num_splits=pa.PA_SPLITS_BY_LENGTH, **skw)
+            lms = time_calls(lfn, steps, warmup, stream)
+            lgbs = byt / (lms * 1e-3) / 1e9
+            res[name + "_by_length"] = {
+                "ms": round(lms, 4), "GB/s": round(lgbs, 1), "frac_of_hbm": round(lgbs / pk["hbm"], 4),
+                "note": "num_splits = PA_SPLITS_BY_LENGTH: rows over 32768 keys cut into parts of "
+                        "2048 keys on the tcgen05 tile kernel"}
+            del lws
         if name.startswith("prefill"):
             # the same row with the part count chosen per call (cut in 3 here)
             aws = pa.make_workspace(pa.make_params(sb.q, sb.k_cache,

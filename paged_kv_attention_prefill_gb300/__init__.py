@@ -26,6 +26,7 @@ import torch
 __all__ = ["paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed",
            "paged_attn_decode_static", "STATIC_SCRATCH_BYTES", "workspace_size",
            "make_workspace", "read_errors", "load", "PagedAttnError", "library_path",
+           "PA_SPLITS_BY_LENGTH", "PA_PREFILL_PARTS_AUTO", "PA_VERIFY_TOKENWISE",
            "PA_F32", "PA_F16", "PA_BF16", "PA_E5M2"]
 
 PA_F32, PA_F16, PA_BF16, PA_E5M2 = 0, 1, 2, 3
@@ -55,6 +56,7 @@ class Params(ctypes.Structure):
 
 PA_VERIFY_PACKED, PA_VERIFY_TOKENWISE = 0, 1
 PA_PREFILL_PARTS_AUTO = -1
+PA_SPLITS_BY_LENGTH = -1
 
 
 class Batch(ctypes.Structure):

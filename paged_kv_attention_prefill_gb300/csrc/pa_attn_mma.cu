@@ -397,14 +397,14 @@ __global__ void __launch_bounds__(128, 1) attn_mma_kernel(const AttnArgs a) {
     for (int w = 0; w < 4; ++w) acc += red[(w * 16 + row) * D + col] * wts[w * 16 + row];
     const int i = R / g, hg = R % g;
     const int64_t slot = slot_base + i;
-    a.part_acc[((slot * Hq + kh * g + hg) * NSPLIT + split) * D + col] = acc;
+    a.part_acc[((slot * Hq + kh * g + hg) * a.split_stride + split) * D + col] = acc;
   }
   if (tid < 16) {
     const int R = r0 + tid;
     if (R < M) {
       const int i = R / g, hg = R % g;
       const int64_t slot = slot_base + i;
-      a.part_ml[(slot * Hq + kh * g + hg) * NSPLIT + split] = make_float2(wts[64 + tid], wts[80 + tid]);
+      a.part_ml[(slot * Hq + kh * g + hg) * a.split_stride + split] = make_float2(wts[64 + tid], wts[80 + tid]);
     }
   }
 }

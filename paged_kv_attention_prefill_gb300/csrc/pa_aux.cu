@@ -173,6 +173,60 @@ cudaError_t launch_plan(const AttnArgs& a, int mode_mixed, int max_decode_q, int
 }
 
 // ---------------------------------------------------------------------------
+// Long-row decode items (PA_SPLITS_BY_LENGTH, one CTA).  Every decode row
+// longer than LONG_MIN_TILES decode tiles contributes one item per split of
+// its length-only partition and per block of LONG_BM GQA-packed query rows:
+// (row | block << 24, split), listed row by row.  The long-row kernel runs
+// each item once per KV head.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) long_items_kernel(const AttnArgs a, int2* items,
+                                                          int64_t max_items) {
+  __shared__ int s_cnt[1024];
+  __shared__ int s_tot;
+  const Problem& p = a.p;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_tot = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < p.num_rows; c0 += 1024) {
+    const int b = c0 + tid;
+    int cnt = 0, nsp = 0, nmb = 0;
+    if (b < p.num_rows) {
+      const int qs = p.cu_q[b], qb = p.cu_q[b + 1] - qs, L = p.seq_lens[b];
+      const bool dec = qb >= 1 && qb <= a.max_decode_q && qs >= 0 && qs + qb <= p.total_q &&
+                       (a.dec_base == nullptr || a.dec_base[b] >= 0);
+      if (dec && dec_is_long(L, 1)) {
+        nsp = dec_num_splits(L, 1);
+        nmb = (qb * p.g + LONG_BM - 1) / LONG_BM;
+        cnt = nsp * nmb;
+      }
+    }
+    s_cnt[tid] = cnt;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int v = tid >= off ? s_cnt[tid - off] : 0;
+      __syncthreads();
+      s_cnt[tid] += v;
+      __syncthreads();
+    }
+    const int64_t o = (int64_t)s_tot + s_cnt[tid] - cnt;
+    for (int k = 0; k < cnt; ++k)
+      if (o + k < max_items) items[o + k] = make_int2(b | ((k % nmb) << 24), k / nmb);
+    __syncthreads();
+    if (tid == 1023) s_tot += s_cnt[1023];
+    __syncthreads();
+  }
+  if (tid == 0)
+    reinterpret_cast<WsHeader*>(p.err)->n_long = (uint32_t)min((int64_t)s_tot, max_items);
+}
+
+cudaError_t launch_long_items(const AttnArgs& a, int2* items, int64_t max_items,
+                              cudaStream_t st) {
+  if (a.p.num_rows >= (1 << 24)) return cudaErrorInvalidValue;
+  long_items_kernel<<<1, 1024, 0, st>>>(a, items, max_items);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Decode work order.  The persistent decode kernel hands out its items
 // (row, KV head, split, row block) in row order; listing the rows whose
 // splits hold the most keys first (longest processing time first) keeps the
@@ -195,8 +249,8 @@ __global__ void __launch_bounds__(1024) row_order_kernel(const AttnArgs a, int32
       unsigned work = 0;
       if (dec) {
         const int L = max(p.seq_lens[i], 0);
-        const int n_tiles = (L + DEC_KT - 1) / DEC_KT;
-        work = (unsigned)((n_tiles + NSPLIT - 1) / NSPLIT) + 1u;
+        // rows on the long-row kernel take no decode-kernel items: last
+        work = a.by_len && dec_is_long(L, 1) ? 0u : (unsigned)dec_split_tiles(L, 0) + 1u;
       }
       key = ((unsigned long long)work << 32) | (unsigned)(n - i);
     }
@@ -215,11 +269,13 @@ cudaError_t launch_row_order(const AttnArgs& a, int32_t* order, cudaStream_t st)
 
 // ---------------------------------------------------------------------------
 // Merge (vllm-rlt PR #128, "Purpose", decode: the second kernel combining the
-// 16 fp32 partial states of a (row, head)).  For one decode token and query
+// fp32 partial states of a (row, head)).  For one decode token and query
 // head: M = max_k m_k over the splits with l_k > 0, w_k = 2^(m_k - M),
 // out = (sum_k w_k acc_k) / (sum_k w_k l_k) * v_scale, summed in the fixed
-// order k = 0..15 so a row's result never depends on the batch.  A token
-// with no visible key gets 0.
+// order k = 0, 1, ... so a row's result never depends on the batch.  A token
+// with no visible key gets 0.  The split count comes from the row's length
+// exactly as the decode kernels cut it: 16, or for a long row under
+// PA_SPLITS_BY_LENGTH up to NSPLIT_MAX.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint32_t* n_slots_dev,
@@ -229,13 +285,13 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
   const int h = blockIdx.y;
   if (n_slots_dev && slot >= (int)*n_slots_dev) return;
   if (slot >= n_slots) return;
-  // The 16 partial states and this thread's accumulator columns are loaded
-  // before the row lookup, so their latency overlaps it: splits past the
-  // row's last (never written: stale bytes) get weight 0 and are not read
-  // further.
+  // The first 16 partial states and this thread's accumulator columns are
+  // loaded before the row lookup, so their latency overlaps it: splits past
+  // the row's last (never written: stale bytes) get weight 0 and are not
+  // read further.
   constexpr int CPT = D / 64;  // accumulator columns per thread
-  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * NSPLIT;
-  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * NSPLIT * D;
+  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * a.split_stride;
+  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * a.split_stride * D;
   float2 mlv[NSPLIT];
   float av[CPT][NSPLIT];
 #pragma unroll
@@ -257,9 +313,44 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
     const int qs = __ldg(p.cu_q + lo), qb = __ldg(p.cu_q + lo + 1) - qs;
     L = L - qb + 1 + (t - qs);
   }
-  const int n_tiles = L > 0 ? (L + DEC_KT - 1) / DEC_KT : 0;
-  const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
-  const int nsp = tps ? (n_tiles + tps - 1) / tps : 0;
+  const int nsp = dec_num_splits(L, a.by_len);
+  T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
+
+  if (nsp > NSPLIT) {
+    // a long row: the same arithmetic over all of its splits, in order
+    float mstar = -INFINITY;
+    for (int k = 0; k < nsp; ++k) {
+      const float2 v = ml[k];
+      if (v.y > 0.f) mstar = fmaxf(mstar, v.x);
+    }
+    float lsum = 0.f, s[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) s[c] = 0.f;
+    for (int k0 = 0; k0 < nsp; k0 += 8) {
+      float2 v[8];
+      float x[CPT][8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u < nsp ? k0 + u : nsp - 1;
+        v[u] = ml[k];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) x[c][u] = acc[(int64_t)k * D + threadIdx.x + 64 * c];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (k0 + u < nsp && v[u].y > 0.f) {
+          const float w = exp2f(v[u].x - mstar);
+          lsum += w * v[u].y;
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) s[c] += w * x[c][u];
+        }
+      }
+    }
+    const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) out[threadIdx.x + 64 * c] = from_float<T>(s[c] * inv);
+    return;
+  }
 
   float mstar = -INFINITY;
 #pragma unroll
@@ -276,7 +367,6 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
     }
   }
   const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-  T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
 #pragma unroll
   for (int c = 0; c < CPT; ++c) {
     float s = 0.f;
@@ -497,7 +587,7 @@ __global__ void __launch_bounds__(128) f32_kernel(const AttnArgs a, int decode_m
     const int i = R / g, hg = R % g;
     if (decode_mode) {
       const int64_t slot = slot_base + i;
-      const int64_t base = (slot * p.hq + kh * g + hg) * NSPLIT + split;
+      const int64_t base = (slot * p.hq + kh * g + hg) * a.split_stride + split;
 #pragma unroll
       for (int e = 0; e < E; ++e) a.part_acc[base * D + lane * E + e] = o[r][e];
       if (lane == 0) a.part_ml[base] = make_float2(m[r], l[r]);

@@ -166,7 +166,14 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
       if (f.slot_base < 0) return false;
     }
     if ((int64_t)f.slot_base + f.qb > a.max_slots) return false;
+    if (f.qb > a.max_decode_q) {
+      // a row too long for the decode path (only the device can see it
+      // without host mirrors): skipped and flagged
+      atomicOr(p.err, PA_DEVERR_DECODE_Q);
+      return false;
+    }
     f.L = __ldg(p.seq_lens + f.b);
+    if (a.by_len && dec_is_long(f.L, 1)) return false;  // on the long-row kernel
   }
   f.M = f.qb * p.g;
   f.r0 = f.mblk * 16;
@@ -577,7 +584,7 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
           const int R = f.r0 + 8 * j + 2 * tig + e;
           if (R >= f.M) continue;
           const int64_t slot = f.slot_base + R / p.g;
-          const int64_t ps = (slot * p.hq + f.kh * p.g + R % p.g) * NSPLIT + f.split;
+          const int64_t ps = (slot * p.hq + f.kh * p.g + R % p.g) * a.split_stride + f.split;
           float* acc = a.part_acc + ps * D;
 #pragma unroll
           for (int m = 0; m < MT; ++m) {

@@ -36,7 +36,8 @@ struct WsHeader {
   uint32_t err;          // sticky PA_DEVERR_* flags
   uint32_t n_tiles;      // prefill work items written by the plan kernel
   uint32_t n_slots;      // decode token slots written by the plan kernel
-  uint32_t pad[61];
+  uint32_t n_long;       // long-row decode work items (PA_SPLITS_BY_LENGTH)
+  uint32_t pad[60];      // [0, 2): the TMA decode kernel's work counter
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -45,17 +46,49 @@ struct WsLayout {
   size_t row_order;  // int32 [num_rows]   decode rows, longest split first
   size_t slot_tok;   // int32 [max_slots]  global token of each decode slot
   size_t tiles;      // int2  [max_tiles]  (row, m-block) prefill work items
-  size_t part_acc;   // float [max_slots, Hq, NSPLIT, d]
-  size_t part_ml;    // float2[max_slots, Hq, NSPLIT]  (m in log2 units, l)
+  size_t part_acc;   // float [max_slots, Hq, split_stride, d]
+  size_t part_ml;    // float2[max_slots, Hq, split_stride]  (m in log2 units, l)
+  size_t long_items; // int2  [max_long]  long-row decode items (row | m-block << 24, split)
   size_t pf_ml;      // float2[total_q, Hq, pf_parts]  prefill key-range parts (0 bytes when off)
   size_t pf_acc;     // float [total_q, Hq, pf_parts, d]
   size_t total;
   int64_t max_slots;
   int64_t max_tiles;
+  int64_t max_long;
+  int split_stride;  // partial states per (decode token, query head)
 };
 
 constexpr int NSPLIT = 16;      // split-KV parts per decode row
 constexpr int DEC_KT = 64;      // keys per decode tile; the split partition unit
+
+// Length-only split count for long rows (num_splits = PA_SPLITS_BY_LENGTH).
+// Rows of at most LONG_MIN_TILES decode tiles (32768 keys) keep the 16-part
+// partition; longer rows get parts of LONG_TPS tiles (2048 keys), at most
+// NSPLIT_MAX of them (longer parts past 262144 keys).  The count depends on
+// the row's length alone (vllm-rlt PR #128, "Purpose", decode bullets: a
+// length-only partition keeps a row's bits independent of the batch).
+constexpr int NSPLIT_MAX = 128;
+constexpr int LONG_MIN_TILES = 512;
+constexpr int LONG_TPS = 32;
+constexpr int LONG_BM = 128;    // GQA-packed query rows per long-row work item
+
+// Decode tiles per split of a row with L keys.
+__host__ __device__ inline int dec_split_tiles(int L, int by_len) {
+  const int n_tiles = L > 0 ? (L + DEC_KT - 1) / DEC_KT : 0;
+  if (!by_len || n_tiles <= LONG_MIN_TILES) return (n_tiles + NSPLIT - 1) / NSPLIT;
+  // an even count, so a long row's parts are whole 128-key tensor-core tiles
+  const int t = ((n_tiles + NSPLIT_MAX - 1) / NSPLIT_MAX + 1) & ~1;
+  return t > LONG_TPS ? t : LONG_TPS;
+}
+// Non-empty splits of a row with L keys.
+__host__ __device__ inline int dec_num_splits(int L, int by_len) {
+  const int tps = dec_split_tiles(L, by_len);
+  return tps ? ((L + DEC_KT - 1) / DEC_KT + tps - 1) / tps : 0;
+}
+// A row whose splits run on the long-row (tcgen05) decode kernel.
+__host__ __device__ inline bool dec_is_long(int L, int by_len) {
+  return by_len && L > LONG_MIN_TILES * DEC_KT;
+}
 constexpr int DEC_ROWS = 16;    // GQA-packed query rows per decode CTA
 constexpr int PF_BM = 64;       // GQA-packed query rows per prefill CTA (mma.sync path)
 
@@ -73,7 +106,7 @@ constexpr int PF_AUTO_MAX = 4;       // the most parts a count chosen per call t
 constexpr int PF_MAX_PARTS = 16;
 
 WsLayout workspace_layout(int num_rows, int total_q, int hq, int d, int max_decode_q, int g,
-                          int pf_parts);
+                          int pf_parts, int by_len);
 
 // Parts of a work item whose rows see keys [0, k_end): sets the units per
 // part and returns the part count (0 for k_end <= 0, 1 when not cut).
@@ -132,6 +165,11 @@ struct AttnArgs {
   int dec_mblk;              // decode grid: 16-row query blocks per row (per token if tokenwise)
   int tokenwise;             // decode rows with q_b > 1 expanded into one-token rows
   const uint32_t* n_slots;   // mixed: decode slots in use (device); null: every token is a slot
+  int split_stride;          // partial states per (decode token, query head): 16 or NSPLIT_MAX
+  int by_len;                // length-only split count for long rows (PA_SPLITS_BY_LENGTH)
+  const int2* long_items;    // long-row decode items (row | m-block << 24, split)
+  const uint32_t* n_long;    // their count (device)
+  int64_t max_long;          // entries the list holds
 };
 
 // Launchers (one per translation unit family).  Return cudaError_t.
@@ -170,6 +208,13 @@ bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
                               int n_units, cudaStream_t st);
 bool decode_mma_supported(int q_dtype, int kv_dtype, int d);
+// Long-row decode (PA_SPLITS_BY_LENGTH): the list of work items of the rows
+// longer than LONG_MIN_TILES decode tiles, then their splits on the tcgen05
+// tile kernel (d = 256, 16-bit q with a same-type cache), which writes the
+// same fp32 partial states as the decode kernel.  `max_items` bounds the list.
+cudaError_t launch_long_items(const AttnArgs& a, int2* items, int64_t max_items,
+                              cudaStream_t st);
+cudaError_t launch_decode_long(const AttnArgs& a, int q_dtype, int grid, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -83,7 +83,7 @@ struct TcCfg {
   static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
 };
 
-template <typename T>
+template <typename T, bool DEC>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -103,35 +103,8 @@ __global__ void __launch_bounds__(384, 1)
   const Problem& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- work item (uniform over the CTA) -----------------------------------
-  // 1-D grid, KV head slowest: CTAs that run together read the same heads'
-  // K/V (L2 reuse); within a head the work list is longest-first
-  const int n_items = (int)(gridDim.x / p.hkv);
-  const int item = blockIdx.x % n_items, kh = blockIdx.x / n_items;
-  if (item >= (int)*a.n_tiles) return;
-  const int2 wi = a.tiles[item];
-  const int b = wi.x, mb = wi.y & 0xFFFFFF, part = wi.y >> 24;
-  const int qs = __ldg(p.cu_q + b);
-  const int qb = __ldg(p.cu_q + b + 1) - qs;
-  const int L = __ldg(p.seq_lens + b);
-  if (qb <= 0) return;
-  if (qs < 0 || qs + qb > p.total_q) {
-    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
-    return;
-  }
-  const int g = p.g, M = qb * g, R0 = mb * C::BM;
-  if (R0 >= M) return;
-  const int r_last = min(R0 + C::BM, M) - 1;
-  const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
-  // the item's key range [k0, k1): the whole range, or one part of it
-  int per_u;
-  const bool cut = pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per_u) > 1;
-  const int k0 = cut ? part * per_u * PF_UNIT : 0;
-  const int k1 = cut ? min(k_end, (part + 1) * per_u * PF_UNIT) : k_end;
-  const int n_tiles = k1 > k0 ? (k1 - k0 + C::BN - 1) / C::BN : 0;
-
   // ---- barriers and TMEM ----------------------------------------------------
-  if (threadIdx.x == 0) {
+  auto init_barriers = [&]() {
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(bar(C::B_KF + s), 1);
       mbar_init(bar(C::B_KE + s), 1);
@@ -148,8 +121,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar(C::B_Q), 8);
     mbar_init(bar(C::B_DRAIN), 1);
-    *abort_flag = 0;
     fence_mbar_init();
+  };
+  if (threadIdx.x == 0) {
+    init_barriers();
+    *abort_flag = 0;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -159,6 +135,79 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // ---- work items ------------------------------------------------------------
+  // Prefill: one item per CTA, a 1-D grid with the KV head slowest (CTAs that
+  // run together read the same heads' K/V: L2 reuse; within a head the work
+  // list is longest-first).
+  // DEC (long-row decode, PA_SPLITS_BY_LENGTH): the CTAs take the (item, KV
+  // head) units of the long-row list in turn; an item is one split of a
+  // decode row's length-only partition for one block of its GQA-packed query
+  // rows, and its result is that split's fp32 partial state (acc, m, l),
+  // written where the decode kernel writes it.  The barriers are made afresh
+  // for every unit after the first; TMEM is held for all of them.
+  const int n_work = DEC ? (int)*a.n_long * p.hkv : 1;
+  int done_units = 0;
+  for (int unit = DEC ? (int)blockIdx.x : 0; unit < n_work;
+       unit += DEC ? (int)gridDim.x : n_work) {
+  int b, mb, part = 0, kh, split = 0;
+  int64_t slot_base = 0;
+  if constexpr (DEC) {
+    const int2 wi = a.long_items[unit / p.hkv];
+    kh = unit % p.hkv;
+    b = wi.x & 0xFFFFFF;
+    mb = wi.x >> 24;
+    split = wi.y;
+  } else {
+    const int n_items = (int)(gridDim.x / p.hkv);
+    const int item = blockIdx.x % n_items;
+    kh = blockIdx.x / n_items;
+    if (item >= (int)*a.n_tiles) continue;
+    const int2 wi = a.tiles[item];
+    b = wi.x;
+    mb = wi.y & 0xFFFFFF;
+    part = wi.y >> 24;
+  }
+  const int qs = __ldg(p.cu_q + b);
+  const int qb = __ldg(p.cu_q + b + 1) - qs;
+  const int L = __ldg(p.seq_lens + b);
+  if (qb <= 0) continue;
+  if (qs < 0 || qs + qb > p.total_q) {
+    if (threadIdx.x == 0) atomicOr(p.err, PA_DEVERR_BAD_PAGE);
+    continue;
+  }
+  const int g = p.g, M = qb * g, R0 = mb * C::BM;
+  if (R0 >= M) continue;
+  int k0, k1;
+  bool cut;
+  if constexpr (DEC) {
+    slot_base = a.dec_base ? (int64_t)__ldg(a.dec_base + b) : (int64_t)qs;
+    if (slot_base < 0 || slot_base + qb > a.max_slots) continue;
+    const int tps = dec_split_tiles(L, 1);
+    k0 = split * tps * DEC_KT;
+    if (k0 >= L) continue;
+    k1 = min(k0 + tps * DEC_KT, L);
+    cut = true;
+  } else {
+    const int r_last = min(R0 + C::BM, M) - 1;
+    const int k_end = min(L, L - qb + r_last / g + 1);  // keys any row of the tile can see
+    // the item's key range [k0, k1): the whole range, or one part of it
+    int per_u;
+    cut = pf_part_count(k_end, a.pf_parts, a.pf_min_units, &per_u) > 1;
+    k0 = cut ? part * per_u * PF_UNIT : 0;
+    k1 = cut ? min(k_end, (part + 1) * per_u * PF_UNIT) : k_end;
+  }
+  const int n_tiles = k1 > k0 ? (k1 - k0 + C::BN - 1) / C::BN : 0;
+  if (DEC && done_units > 0) {
+    // every role is past the previous unit's last barrier operation (the
+    // block-wide barrier at its end): make the barriers afresh
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < C::NBAR; ++i) mbar_inval(bar(i));
+      init_barriers();
+    }
+    __syncthreads();
+  }
+  ++done_units;
 
   if (warp == 0 || warp == 2) {
     // ============== producers: warp 0 streams K tiles, warp 2 V halves =======
@@ -241,6 +290,11 @@ __global__ void __launch_bounds__(384, 1)
       // copies this warp started may still be landing: wait for them
       for (int uu = max(0, u - NS); uu < u; ++uu)
         mbar_drain(bar(B_FULL + uu % NS), (uu / NS) & 1, p.err);
+    } else if (DEC) {
+      // the barriers are made afresh for the next unit: first let the
+      // products release the last stages (their commits arrive here)
+      for (int uu = max(0, n_units - NS); uu < n_units; ++uu)
+        mbar_wait(bar(B_EMPTY + uu % NS), (uu / NS) & 1, abort_flag, p.err);
     }
   } else if (warp == 1) {
     // ======================= MMA issuer (one thread) =======================
@@ -318,7 +372,8 @@ __global__ void __launch_bounds__(384, 1)
     const int R = R0 + r;
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
-    const int last = valid ? L - qb + i - k0 : -1 - k0;  // last visible key, from k0
+    // last visible key, from k0 (a decode split also ends at k1)
+    const int last = valid ? min(L - qb + i, k1 - 1) - k0 : -1 - k0;
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     {
@@ -447,11 +502,15 @@ __global__ void __launch_bounds__(384, 1)
     T* orow = static_cast<T*>(a.out) + qoff + hf * HD;
     if (cut) {
       // this part's unnormalised O (each warpgroup its d / 2 columns), the
-      // maximum it is relative to and the row sum, for the merge
-      const int64_t slot = ((int64_t)(qs + i) * p.hq + kh * g + hg) * a.pf_parts + part;
+      // maximum it is relative to and the row sum, for the merge: a prefill
+      // key-range part, or a decode split (in the decode kernel's layout)
+      const int64_t slot =
+          DEC ? ((slot_base + i) * p.hq + kh * g + hg) * a.split_stride + split
+              : ((int64_t)(qs + i) * p.hq + kh * g + hg) * a.pf_parts + part;
+      float2* mlp = DEC ? a.part_ml : a.pf_ml;
       if (valid && hf == 0)
-        a.pf_ml[slot] = make_float2(n_tiles > 0 ? m_used : -INFINITY, n_tiles > 0 ? lt : 0.f);
-      float* prow = a.pf_acc + slot * D + hf * HD;
+        mlp[slot] = make_float2(n_tiles > 0 ? m_used : -INFINITY, n_tiles > 0 ? lt : 0.f);
+      float* prow = (DEC ? a.part_acc : a.pf_acc) + slot * D + hf * HD;
       if (n_tiles > 0) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
@@ -493,6 +552,8 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  }  // work items
+
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -1050,7 +1111,7 @@ namespace {
 template <typename T>
 cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
                       bool kv8, cudaStream_t st) {
-  auto k = kv8 ? prefill_tc8_kernel<T> : prefill_tc_kernel<T>;
+  auto k = kv8 ? prefill_tc8_kernel<T> : prefill_tc_kernel<T, false>;
   const uint32_t smem = kv8 ? Tc8Cfg::SMEM : TcCfg::SMEM;
   static DeviceFlags attr16, attr8;
   cudaError_t e = (kv8 ? attr8 : attr16).once([&] {
@@ -1062,6 +1123,37 @@ cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMa
 }
 
 }  // namespace
+
+namespace {
+
+// The long-row decode splits on the same kernel (one CTA per SM at most; the
+// CTAs take the list's (item, KV head) units in turn).
+template <typename T>
+cudaError_t launch_tc_long(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                           int grid, cudaStream_t st) {
+  auto k = prefill_tc_kernel<T, true>;
+  static DeviceFlags attr;
+  cudaError_t e = attr.once([&] {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
+  });
+  if (e != cudaSuccess) return e;
+  k<<<dim3((unsigned)grid), 384, TcCfg::SMEM, st>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_long(const AttnArgs& a, int q_dtype, int grid, cudaStream_t st) {
+  if (grid <= 0) return cudaSuccess;
+  if (a.p.d != 256) return cudaErrorInvalidValue;
+  const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
+  CUtensorMap tk, tv;
+  if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+    return cudaErrorInvalidValue;
+  return q_dtype == PA_BF16 ? launch_tc_long<__nv_bfloat16>(a, tk, tv, grid, st)
+                            : launch_tc_long<__half>(a, tk, tv, grid, st);
+}
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
   return (q_dtype == PA_BF16 || q_dtype == PA_F16) && (kv_dtype == q_dtype || kv_dtype == PA_E5M2) &&

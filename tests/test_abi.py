@@ -66,6 +66,33 @@ def test_workspace_matches_the_decode_workspace_figure(lib):
     assert lib.paged_attn_workspace_size(None, 4, 4) == 0
 
 
+def test_length_only_split_workspace_and_checks(lib):
+    # PA_SPLITS_BY_LENGTH: 128 partial states per decode token and head (the
+    # default's 16 times 8) plus the long-row item list; other modes refused
+    by_len = pa.PA_SPLITS_BY_LENGTH
+    p16 = params(num_q_heads=24, num_kv_heads=4, head_dim=256, q_dtype=pa.PA_F16,
+                 kv_dtype=pa.PA_F16)
+    plen = params(num_q_heads=24, num_kv_heads=4, head_dim=256, q_dtype=pa.PA_F16,
+                  kv_dtype=pa.PA_F16, num_splits=by_len)
+    n16, nlen = pa.workspace_size(p16, 8, 40), pa.workspace_size(plen, 8, 40)
+    per_split = 24 * (256 + 2) * 4          # one split of one token, all heads
+    items = 8 * 128 * 1 * 8                 # rows x splits x 128-row blocks x int2
+    assert nlen - n16 >= 40 * (128 - 16) * per_split + items
+    assert nlen - n16 <= 40 * (128 - 16) * per_split + items + 4 * 256
+    assert lib.paged_attn_workspace_size(ctypes.byref(params(num_splits=-2)), 4, 4) == 0
+    for name in ("paged_attn_decode", "paged_attn_mixed"):
+        # built for d = 256 with a 16-bit same-type cache and packed verify rows
+        for p in (params(num_splits=by_len),
+                  params(head_dim=256, q_dtype=pa.PA_F16, kv_dtype=pa.PA_E5M2,
+                         num_splits=by_len),
+                  params(head_dim=256, q_dtype=pa.PA_F32, kv_dtype=pa.PA_F32,
+                         num_splits=by_len),
+                  params(head_dim=256, num_splits=by_len,
+                         verify_mode=pa.PA_VERIFY_TOKENWISE)):
+            assert FakeCall(lib, p, [1, 1], [10, 20])(name) == UNSUPPORTED
+        assert FakeCall(lib, params(num_splits=-2), [1, 1], [10, 20])(name) == UNSUPPORTED
+
+
 class FakeCall:
     """Builds argument structs with non-null dummy pointers.  They are never
     dereferenced: every case either fails validation before any launch or,
