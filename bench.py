@@ -400,10 +400,42 @@ def part_small1(steps, warmup, stream):
         pa.paged_attn_decode_static(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
                                     b.seq_lens, out=out, **kw)
     ms_graph = graph_ms(fn_static, steps, warmup, stream)
+    host_us = host_us_per_call(b, ws, out)
     return {"workload": workloads.WORKLOADS[1], "us_per_call": round(ms * 1e3, 2),
             "graph_replay_us_per_call": round(ms_graph * 1e3, 2),
+            "host_us_per_call": host_us,
+            "host_note": "wall time of the C ABI call itself (argument checks, tensor-map "
+                         "encoding, launches), from a loop of ctypes calls with argument "
+                         "structs built once, no stream sync inside the loop; median of "
+                         "10 loops of 100 calls",
             "note": "launch-latency bound (0.59 MB); the graph holds paged_attn_decode_static "
                     "(no workspace argument)"}
+
+
+def host_us_per_call(b, ws, out, calls=100, loops=10):
+    """Host-side cost of one paged_attn_decode call through the C ABI."""
+    import ctypes
+    import paged_kv_attention_prefill_gb300 as pa
+    lib = pa.load()
+    prm = pa.make_params(b.q, b.k_cache, softmax_scale=b.softmax_scale, k_scale=b.k_scale,
+                         v_scale=b.v_scale)
+    cu_h, lens_h = b.cu_seqlens_q.cpu().contiguous(), b.seq_lens.cpu().contiguous()
+    bat = pa.Batch(b.num_rows, b.total_q, b.num_pages, int(b.block_table.shape[1]),
+                   b.cu_seqlens_q.data_ptr(), b.seq_lens.data_ptr(), b.block_table.data_ptr(),
+                   cu_h.data_ptr(), lens_h.data_ptr())
+    fn = lib.paged_attn_decode
+    args = (ctypes.byref(prm), ctypes.byref(bat), b.q.data_ptr(), b.k_cache.data_ptr(),
+            b.v_cache.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
+            torch.cuda.current_stream().cuda_stream)
+    per = []
+    for _ in range(loops + 1):
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(calls):
+            fn(*args)
+        per.append((time.perf_counter() - t) / calls * 1e6)
+        torch.cuda.synchronize()
+    return round(statistics.median(per[1:]), 2)
 
 
 def cpu_baseline_sample(b, budget_s=12.0, one_thread=True):

@@ -71,6 +71,31 @@ def library_path() -> str:
     return _LIB_PATH
 
 
+def load_library(path: str):
+    """A copy of the C library at `path` with its function signatures
+    declared (the package itself uses load(); tests also load test builds)."""
+    lib = ctypes.CDLL(path)
+    P, B = ctypes.POINTER(Params), ctypes.POINTER(Batch)
+    for name in ("paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.paged_attn_decode_static.restype = ctypes.c_int
+    lib.paged_attn_decode_static.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p]
+    lib.paged_attn_workspace_size.restype = ctypes.c_size_t
+    lib.paged_attn_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.c_int32]
+    lib.paged_attn_read_errors.restype = ctypes.c_int
+    lib.paged_attn_read_errors.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.POINTER(ctypes.c_uint32)]
+    lib.paged_attn_status_string.restype = ctypes.c_char_p
+    lib.paged_attn_status_string.argtypes = [ctypes.c_int]
+    lib.paged_attn_version.restype = ctypes.c_int32
+    return lib
+
+
 def load():
     """The loaded C library; raises if it has not been built."""
     global _lib
@@ -80,26 +105,7 @@ def load():
                 raise PagedAttnError(
                     f"paged attention CUDA library missing at {_LIB_PATH}; "
                     "build it with paged_kv_attention_prefill_gb300.build.build()")
-            lib = ctypes.CDLL(_LIB_PATH)
-            P, B = ctypes.POINTER(Params), ctypes.POINTER(Batch)
-            for name in ("paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed"):
-                f = getattr(lib, name)
-                f.restype = ctypes.c_int
-                f.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
-            lib.paged_attn_decode_static.restype = ctypes.c_int
-            lib.paged_attn_decode_static.argtypes = [P, B, ctypes.c_void_p, ctypes.c_void_p,
-                                                     ctypes.c_void_p, ctypes.c_void_p,
-                                                     ctypes.c_void_p]
-            lib.paged_attn_workspace_size.restype = ctypes.c_size_t
-            lib.paged_attn_workspace_size.argtypes = [P, ctypes.c_int32, ctypes.c_int32]
-            lib.paged_attn_read_errors.restype = ctypes.c_int
-            lib.paged_attn_read_errors.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
-                                                   ctypes.POINTER(ctypes.c_uint32)]
-            lib.paged_attn_status_string.restype = ctypes.c_char_p
-            lib.paged_attn_status_string.argtypes = [ctypes.c_int]
-            lib.paged_attn_version.restype = ctypes.c_int32
-            _lib = lib
+            _lib = load_library(_LIB_PATH)
     return _lib
 
 

@@ -80,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, in
   for (uint32_t it = 0;; ++it) {
     const bool ok = mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
-    if ((it & 63u) == 63u) {
+    if ((it & WAIT_CHECK_MASK) == WAIT_CHECK_MASK) {
       const int late = __shfl_sync(0xffffffffu, (int)(clock64() - t0 > WAIT_LIMIT_CYCLES), 0);
       if (late) {
         if (lane == 0) atomicOr(err, PA_DEVERR_TIMEOUT);

@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(384, 1)
       const int P = p.page_size;
       const int64_t bt_row = (int64_t)b * p.max_pages;
       int j = 0;
+      int started[2] = {0, 0};  // K / V code units whose copies were started
       bool ok = true;
       for (; j < n_kv; ++j) {
         const int st = j % C::S8;
@@ -267,15 +268,17 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_tma * 16u * 128u);
           __syncwarp();
           if (kind == 1) tma_load_3d(dst + lane * 16 * 128, kv ? (const void*)&tmV : (const void*)&tmK, 0, kh, tok0, fb);
+          ++started[kv];
         }
         if (!ok) break;
       }
       if (!ok) {
-        // copies this warp started may still be landing: wait for them
-        for (int jj = max(0, j - C::S8); jj <= j && jj < n_kv; ++jj) {
-          mbar_drain(bar(C::B_K8F + jj % C::S8), (jj / C::S8) & 1, p.err);
-          if (jj < j) mbar_drain(bar(C::B_V8F + jj % C::S8), (jj / C::S8) & 1, p.err);
-        }
+        // copies this warp started may still be landing: wait for them (the
+        // last S8 units of each ring; earlier ones were consumed already)
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+          for (int jj = max(0, started[kv] - C::S8); jj < started[kv]; ++jj)
+            mbar_drain(bar((kv ? C::B_V8F : C::B_K8F) + jj % C::S8), (jj / C::S8) & 1, p.err);
       }
     } else if (KV8 && (warp == 2 || warp == 3)) {
       // ===== fp8 cache: warps 2 and 3 widen every K and V tile =================

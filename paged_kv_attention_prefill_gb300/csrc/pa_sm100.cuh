@@ -33,21 +33,48 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
                "r"(tx)
                : "memory");
 }
+// One poll of the phase with the given parity.  try_wait may suspend the
+// thread for a while before it answers; a build with PA_WAIT_POLL_ONLY polls
+// with test_wait, which answers at once (the timeout-path test's build, so
+// that even short waits run past its tiny limit).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#ifdef PA_WAIT_POLL_ONLY
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#else
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 
 // About two seconds at the top SM clock: far beyond any legitimate wait in
 // these kernels, short enough that a lost arrival ends the kernel with an
-// error flag instead of a hang.
-constexpr long long WAIT_LIMIT_CYCLES = 4000000000ll;
+// error flag instead of a hang.  A build may lower the limit after which a
+// wait gives up (PA_WAIT_LIMIT_CYCLES) so that waits run out on purpose: the
+// library's test of the timeout path does so in a build of its own.  Drains
+// keep the full limit, so the copies and MMAs a CTA started still land
+// before it frees its resources and exits.
+#ifndef PA_WAIT_LIMIT_CYCLES
+#define PA_WAIT_LIMIT_CYCLES 4000000000ll
+#endif
+// polls of the barrier between two looks at the clock (a power of two)
+#ifndef PA_WAIT_CHECK_EVERY
+#define PA_WAIT_CHECK_EVERY 64u
+#endif
+constexpr long long WAIT_LIMIT_CYCLES = PA_WAIT_LIMIT_CYCLES;
+constexpr long long DRAIN_LIMIT_CYCLES = 4000000000ll;
+constexpr uint32_t WAIT_CHECK_MASK = PA_WAIT_CHECK_EVERY - 1u;
+static_assert((PA_WAIT_CHECK_EVERY & WAIT_CHECK_MASK) == 0, "a power of two");
 
 // Waits for the phase with the given parity.  Returns false (and raises the
 // CTA's abort flag and the workspace timeout flag) if the wait runs past
@@ -58,7 +85,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & WAIT_CHECK_MASK) == 0) {
       if (*abort_flag) return false;
       if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
         *abort_flag = 1;
@@ -74,7 +101,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint32_t* err) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > DRAIN_LIMIT_CYCLES) {
       atomicOr(err, PA_DEVERR_TIMEOUT);
       return;
     }
