@@ -399,17 +399,30 @@ def part_small1(steps, warmup, stream):
     def fn_static():
         pa.paged_attn_decode_static(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
                                     b.seq_lens, out=out, **kw)
-    ms_graph = graph_ms(fn_static, steps, warmup, stream)
+    ms_graph = graph_ms(fn, steps, warmup, stream)
+    ms_static_graph = graph_ms(fn_static, steps, warmup, stream)
     host_us = host_us_per_call(b, ws, out)
+
+    def fn_sep():
+        pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                             b.seq_lens, out=out, workspace=ws,
+                             merge_mode=pa.PA_MERGE_SEPARATE, **kw)
+    ms_sep = time_calls(fn_sep, steps, warmup, stream)
+    ms_sep_graph = graph_ms(fn_sep, steps, warmup, stream)
     return {"workload": workloads.WORKLOADS[1], "us_per_call": round(ms * 1e3, 2),
             "graph_replay_us_per_call": round(ms_graph * 1e3, 2),
+            "merge": "in the decode launch (PA_MERGE_AUTO picks it: the grid is smaller than "
+                     "the GPU)",
+            "separate_merge_us_per_call": round(ms_sep * 1e3, 2),
+            "separate_merge_graph_replay_us_per_call": round(ms_sep_graph * 1e3, 2),
+            "static_entry_graph_replay_us_per_call": round(ms_static_graph * 1e3, 2),
             "host_us_per_call": host_us,
             "host_note": "wall time of the C ABI call itself (argument checks, tensor-map "
                          "encoding, launches), from a loop of ctypes calls with argument "
                          "structs built once, no stream sync inside the loop; median of "
                          "10 loops of 100 calls",
-            "note": "launch-latency bound (0.59 MB); the graph holds paged_attn_decode_static "
-                    "(no workspace argument)"}
+            "note": "launch-latency bound (0.59 MB); paged_attn_decode_static (no workspace "
+                    "argument) clears its array's work counters with a memset node first"}
 
 
 def host_us_per_call(b, ws, out, calls=100, loops=10):

@@ -129,7 +129,25 @@ typedef struct pa_params {
                                0 or 1 = not cut, 2..16 = at most this many
                                parts, PA_PREFILL_PARTS_AUTO = chosen per
                                call, see below */
+  int32_t merge_mode;     /* split-KV merge of paged_attn_decode: PA_MERGE_AUTO
+                             (0), PA_MERGE_SEPARATE or PA_MERGE_SAME_LAUNCH,
+                             see below */
 } pa_params;
+
+/*
+ * Where the split-KV merge of paged_attn_decode (and _decode_static) runs
+ * (vllm-rlt PR #128, Test Result: a follow-up merges inside the decode
+ * launch, bitwise identical to the two-kernel path, to save host time per
+ * call).  PA_MERGE_SEPARATE: a second kernel.  PA_MERGE_SAME_LAUNCH: the
+ * decode kernel itself, after a grid-wide barrier (its CTAs, at most one per
+ * SM, wait for each other with the clock bound every wait has).
+ * PA_MERGE_AUTO: the same launch when the decode grid is smaller than the
+ * GPU (small batches, where the second launch costs more than the merge),
+ * otherwise separate.  The result is the same bits either way.  Applies to
+ * the TMA decode kernel (16-bit q) without PA_SPLITS_BY_LENGTH; other
+ * decode paths, and the mixed call, always merge in a separate kernel.
+ */
+enum { PA_MERGE_AUTO = 0, PA_MERGE_SEPARATE = 1, PA_MERGE_SAME_LAUNCH = 2 };
 
 /*
  * Decode rows with q_b > 1 (speculative-verify rows):

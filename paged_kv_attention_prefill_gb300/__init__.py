@@ -27,6 +27,7 @@ __all__ = ["paged_attn_prefill", "paged_attn_decode", "paged_attn_mixed",
            "paged_attn_decode_static", "STATIC_SCRATCH_BYTES", "workspace_size",
            "make_workspace", "read_errors", "load", "PagedAttnError", "library_path",
            "PA_SPLITS_BY_LENGTH", "PA_PREFILL_PARTS_AUTO", "PA_VERIFY_TOKENWISE",
+           "PA_MERGE_AUTO", "PA_MERGE_SEPARATE", "PA_MERGE_SAME_LAUNCH",
            "PA_F32", "PA_F16", "PA_BF16", "PA_E5M2"]
 
 PA_F32, PA_F16, PA_BF16, PA_E5M2 = 0, 1, 2, 3
@@ -52,11 +53,12 @@ class Params(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float), ("max_decode_q", ctypes.c_int32),
                 ("num_splits", ctypes.c_int32), ("verify_mode", ctypes.c_int32),
-                ("prefill_kv_parts", ctypes.c_int32)]
+                ("prefill_kv_parts", ctypes.c_int32), ("merge_mode", ctypes.c_int32)]
 
 PA_VERIFY_PACKED, PA_VERIFY_TOKENWISE = 0, 1
 PA_PREFILL_PARTS_AUTO = -1
 PA_SPLITS_BY_LENGTH = -1
+PA_MERGE_AUTO, PA_MERGE_SEPARATE, PA_MERGE_SAME_LAUNCH = 0, 1, 2
 
 
 class Batch(ctypes.Structure):
@@ -122,11 +124,13 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def make_params(q, k_cache, *, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
-                num_splits=0, verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0) -> Params:
+                num_splits=0, verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0,
+                merge_mode=PA_MERGE_AUTO) -> Params:
     return Params(int(q.shape[1]), int(k_cache.shape[2]), int(q.shape[2]),
                   int(k_cache.shape[1]), _dtype_code(q), _dtype_code(k_cache),
                   float(softmax_scale or 0.0), float(k_scale), float(v_scale),
-                  int(max_decode_q), int(num_splits), int(verify_mode), int(prefill_kv_parts))
+                  int(max_decode_q), int(num_splits), int(verify_mode), int(prefill_kv_parts),
+                  int(merge_mode))
 
 
 def workspace_size(params: Params, num_rows: int, total_q: int) -> int:
@@ -155,7 +159,7 @@ def _ptr(t: Optional[torch.Tensor]):
 def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out=None,
           workspace=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0, max_decode_q=0,
           num_splits=0, verify_mode=PA_VERIFY_PACKED, prefill_kv_parts=0,
-          cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
+          merge_mode=PA_MERGE_AUTO, cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
     for t in (q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens):
         if not t.is_cuda:
             raise PagedAttnError("all tensors must be CUDA tensors")
@@ -166,7 +170,8 @@ def _call(name, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *, out
         raise PagedAttnError("block_table, cu_seqlens_q and seq_lens must be int32")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
                       v_scale=v_scale, max_decode_q=max_decode_q, num_splits=num_splits,
-                      verify_mode=verify_mode, prefill_kv_parts=prefill_kv_parts)
+                      verify_mode=verify_mode, prefill_kv_parts=prefill_kv_parts,
+                      merge_mode=merge_mode)
     B = int(seq_lens.shape[0])
     total_q = int(q.shape[0])
     if out is None:
@@ -211,7 +216,8 @@ def paged_attn_mixed(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *
 def paged_attn_decode_static(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, *,
                              out=None, softmax_scale=0.0, k_scale=1.0, v_scale=1.0,
                              max_decode_q=0, verify_mode=PA_VERIFY_PACKED,
-                             cu_seqlens_q_host=None, seq_lens_host=None, stream=None):
+                             merge_mode=PA_MERGE_AUTO, cu_seqlens_q_host=None,
+                             seq_lens_host=None, stream=None):
     """Split-KV decode without a workspace: for callers that cannot allocate
     device memory.  The library's fixed device array (STATIC_SCRATCH_BYTES,
     shared by every call) holds the scratch; larger batches are refused.
@@ -220,7 +226,8 @@ def paged_attn_decode_static(q, k_cache, v_cache, block_table, cu_seqlens_q, seq
         if not t.is_cuda or not t.is_contiguous():
             raise PagedAttnError("all tensors must be contiguous CUDA tensors")
     prm = make_params(q, k_cache, softmax_scale=softmax_scale, k_scale=k_scale,
-                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode)
+                      v_scale=v_scale, max_decode_q=max_decode_q, verify_mode=verify_mode,
+                      merge_mode=merge_mode)
     B = int(seq_lens.shape[0])
     if out is None:
         out = torch.empty_like(q)

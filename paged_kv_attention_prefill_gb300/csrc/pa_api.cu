@@ -78,6 +78,7 @@ struct Resolved {
   bool long_tc;       // long decode rows on the tcgen05 kernel
   int host_long;      // long-row decode work items (host mirrors)
   int host_short;     // decode rows on the decode kernel (host mirrors)
+  int merge_mode;     // PA_MERGE_*
 };
 
 // 0 = not checked, 1 = sm_103, 2 = other
@@ -115,6 +116,10 @@ pa_status resolve_params(const pa_params* prm, Resolved* r) {
       prm->num_splits != PA_SPLITS_BY_LENGTH)
     return PA_ERR_UNSUPPORTED;
   r->by_len = prm->num_splits == PA_SPLITS_BY_LENGTH;
+  if (prm->merge_mode != PA_MERGE_AUTO && prm->merge_mode != PA_MERGE_SEPARATE &&
+      prm->merge_mode != PA_MERGE_SAME_LAUNCH)
+    return PA_ERR_INVALID_ARG;
+  r->merge_mode = prm->merge_mode;
   if (prm->max_decode_q < 0) return PA_ERR_INVALID_ARG;
   if (!(std::isfinite(prm->softmax_scale) && std::isfinite(prm->k_scale) &&
         std::isfinite(prm->v_scale)))
@@ -397,7 +402,7 @@ int decode_mblocks(const Resolved& r, int max_q) {
 constexpr int ORDER_MIN_ROWS = 16;
 
 cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_slots,
-                       int32_t* order, cudaStream_t st) {
+                       int32_t* order, bool same_launch_ok, cudaStream_t st) {
   AttnArgs a = a0;
   a.dec_mblk = n_mblk;
   cudaError_t e = cudaSuccess;
@@ -424,7 +429,18 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
     // packed: work items range over rows; tokenwise: over decode slots
     const int units = r.tokenwise ? (int)std::min<int64_t>(a.p.total_q, a.max_slots)
                                   : a.p.num_rows;
-    e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, units, st);
+    // the merge in the same launch: asked for, or (by default) when the
+    // decode grid leaves SMs idle, so the second launch would cost more
+    const int sms = sm_count();
+    int merge_slots = 0;
+    if (same_launch_ok && !r.long_tc && r.merge_mode != PA_MERGE_SEPARATE) {
+      const int64_t items = (int64_t)units * r.hkv * NSPLIT * n_mblk;
+      if (r.merge_mode == PA_MERGE_SAME_LAUNCH ||
+          decode_tma_grid(r.d, r.kvd == PA_E5M2, items, sms) < sms)
+        merge_slots = n_slots;
+    }
+    e = launch_decode_tma(a, r.qd, r.kvd, n_mblk, units, merge_slots, sms, st);
+    if (e == cudaSuccess && merge_slots > 0) return e;
   } else
     e = launch_decode_mma(a, r.qd, r.kvd, n_mblk, st);
   if (e != cudaSuccess) return e;
@@ -492,7 +508,7 @@ pa_status paged_attn_decode(const pa_params* params, const pa_batch* batch, cons
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
   return cuda_status(run_decode(a, r, decode_mblocks(r, max_q), n_slots,
-                                row_order_of(workspace, batch, r), st));
+                                row_order_of(workspace, batch, r), true, st));
 }
 
 pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const void* q,
@@ -538,7 +554,7 @@ pa_status paged_attn_mixed(const pa_params* params, const pa_batch* batch, const
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (max_q > 0) {
     e = run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(workspace, batch, r),
-                   dst);
+                   false, dst);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   if (aux && cudaEventRecord(aux->join, aux->st) != cudaSuccess) return PA_ERR_CUDA;
@@ -575,7 +591,7 @@ const char* paged_attn_status_string(pa_status status) {
   return "unknown status";
 }
 
-int32_t paged_attn_version(void) { return 100; }
+int32_t paged_attn_version(void) { return 200; }
 
 }  // extern "C"
 
@@ -688,5 +704,5 @@ extern "C" pa_status paged_attn_decode_static(const pa_params* params, const pa_
   const int max_q = r.host ? r.host_max_q_dec : r.max_dq;
   const int n_slots = (int)std::min<int64_t>(batch->total_q, a.max_slots);
   return cuda_status(
-      run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(ws, batch, r), st));
+      run_decode(a, r, decode_mblocks(r, max_q), n_slots, row_order_of(ws, batch, r), true, st));
 }

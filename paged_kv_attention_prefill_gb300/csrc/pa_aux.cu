@@ -301,19 +301,7 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
     for (int c = 0; c < CPT; ++c) av[c][k] = acc[k * D + threadIdx.x + 64 * c];
   }
   const int t = a.slot_tok ? a.slot_tok[slot] : slot;
-  // row of token t: largest b with cu_q[b] <= t
-  int lo = 0, hi = p.num_rows - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  int L = __ldg(p.seq_lens + lo);
-  if (a.tokenwise) {
-    // a one-token row: its own length, so its own partition
-    const int qs = __ldg(p.cu_q + lo), qb = __ldg(p.cu_q + lo + 1) - qs;
-    L = L - qb + 1 + (t - qs);
-  }
-  const int nsp = dec_num_splits(L, a.by_len);
+  const int nsp = merge_splits(a, t);
   T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D;
 
   if (nsp > NSPLIT) {
@@ -352,29 +340,10 @@ __global__ void __launch_bounds__(64) merge_kernel(const AttnArgs a, const uint3
     return;
   }
 
-  float mstar = -INFINITY;
+  float res[CPT];
+  merge16<CPT>(mlv, av, nsp, p.v_scale, res);
 #pragma unroll
-  for (int k = 0; k < NSPLIT; ++k)
-    if (k < nsp && mlv[k].y > 0.f) mstar = fmaxf(mstar, mlv[k].x);
-  float w[NSPLIT];
-  float lsum = 0.f;
-#pragma unroll
-  for (int k = 0; k < NSPLIT; ++k) {
-    w[k] = 0.f;
-    if (k < nsp && mlv[k].y > 0.f) {
-      w[k] = exp2f(mlv[k].x - mstar);
-      lsum += w[k] * mlv[k].y;
-    }
-  }
-  const float inv = lsum > 0.f ? p.v_scale / lsum : 0.f;
-#pragma unroll
-  for (int c = 0; c < CPT; ++c) {
-    float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < NSPLIT; ++k)
-      if (w[k] != 0.f) s += w[k] * av[c][k];
-    out[threadIdx.x + 64 * c] = from_float<T>(s * inv);
-  }
+  for (int c = 0; c < CPT; ++c) out[threadIdx.x + 64 * c] = from_float<T>(res[c]);
 }
 
 cudaError_t launch_merge(const AttnArgs& a, int q_dtype, int n_slots, cudaStream_t st) {

@@ -187,11 +187,47 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
   return true;
 }
 
-template <typename T, bool KV8, int D>
+// Same-launch merge (FUSED; vllm-rlt PR #128, Test Result: a follow-up
+// merges inside the decode launch, bitwise equal to the two-kernel path).
+// Once its items are done, every warp arrives at a grid-wide barrier (a
+// counter in the workspace, waited on with the same clock bound as every
+// other wait); then the warps take the (decode token, query head) pairs in
+// turn and merge each with the merge kernel's arithmetic (merge16), lane =
+// D / 32 consecutive head-dim columns.  Used for decode calls whose grid is
+// smaller than the GPU, where the second launch costs more than the merge.
+template <typename T, int D>
+__device__ __forceinline__ void merge_pair(const AttnArgs& a, int slot, int h, int lane) {
+  constexpr int NC = D / 32;
+  const Problem& p = a.p;
+  const float2* ml = a.part_ml + ((int64_t)slot * p.hq + h) * a.split_stride;
+  const float* acc = a.part_acc + ((int64_t)slot * p.hq + h) * a.split_stride * D + lane * NC;
+  float2 mlv[NSPLIT];
+  float av[NC][NSPLIT];
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k) {
+    // L2 loads: the states were written by other SMs in this launch
+    mlv[k] = __ldcg(ml + k);
+#pragma unroll
+    for (int c = 0; c < NC; c += 2) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(acc + (int64_t)k * D + c));
+      av[c][k] = v.x;
+      av[c + 1][k] = v.y;
+    }
+  }
+  const int t = a.slot_tok ? __ldg(a.slot_tok + slot) : slot;
+  float res[NC];
+  merge16<NC>(mlv, av, merge_splits(a, t), p.v_scale, res);
+  T* out = static_cast<T*>(a.out) + ((int64_t)t * p.hq + h) * D + lane * NC;
+#pragma unroll
+  for (int c = 0; c < NC; c += 2)
+    *reinterpret_cast<uint32_t*>(out + c) = pack2<T>(res[c], res[c + 1]);
+}
+
+template <typename T, bool KV8, int D, bool FUSED>
 __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
     decode_tma_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, int total_items, int n_mblk,
-                      uint32_t* counters) {
+                      uint32_t* counters, int merge_slots) {
   using C = DecCfg<D, KV8>;
   constexpr int NS = C::NS;
   constexpr int KSTEPS = D / 16;  // 16-wide reduction steps of S over the head dim
@@ -614,47 +650,86 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
       if (meta[s].x >= 0) mbar_drain(bar0 + 8 * s, (phase >> s) & 1u, p.err);
   }
   __syncwarp();
-  // the last warp of the grid resets the item counter for the next call
+  const uint32_t n_warps = gridDim.x * C::W;
+  if constexpr (FUSED) {
+    // grid-wide barrier: every warp's partial states are written.  One
+    // arrival per CTA, once all of its warps are done with their items.
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int ok = 1;
+      // cumulative: releases the writes of the whole CTA (ordered before it
+      // by the block barrier) to the CTAs that see the arrival
+      __threadfence();
+      atomicAdd(counters + 2, 1u);
+      const long long t0 = clock64();
+      while (*reinterpret_cast<volatile uint32_t*>(counters + 2) < gridDim.x) {
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+          atomicOr(p.err, PA_DEVERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+      __threadfence();
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (s_ok) {
+      const int n_pairs = merge_slots * p.hq;
+      for (int u = blockIdx.x * C::W + warp; u < n_pairs; u += (int)n_warps)
+        merge_pair<T, D>(a, u / p.hq, u % p.hq, lane);
+    }
+    __syncwarp();
+  }
+  // the last warp of the grid resets the counters for the next call
   if (lane == 0) {
     __threadfence();
     const uint32_t done = atomicAdd(counters + 1, 1u);
-    if (done == gridDim.x * C::W - 1) {
+    if (done == n_warps - 1) {
       counters[0] = 0u;
       counters[1] = 0u;
+      counters[2] = 0u;
       __threadfence();
     }
   }
 }
 
+template <int D, bool KV8>
+int dec_grid(int total_items, int sms) {
+  using C = DecCfg<D, KV8>;
+  int grid = sms > 0 ? sms : 148;  // persistent: one CTA per SM
+  if (total_items < grid * C::W) grid = (total_items + C::W - 1) / C::W;
+  return grid < 1 ? 1 : grid;
+}
+
 template <typename T, bool KV8, int D>
 cudaError_t launch_dec(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                       int total_items, int n_mblk, uint32_t* counters, cudaStream_t st) {
+                       int total_items, int n_mblk, uint32_t* counters, int merge_slots,
+                       int sms, cudaStream_t st) {
   using C = DecCfg<D, KV8>;
-  auto k = decode_tma_kernel<T, KV8, D>;
-  static DeviceFlags attr;
-  cudaError_t e = attr.once([&] {
+  auto k = merge_slots > 0 ? decode_tma_kernel<T, KV8, D, true>
+                           : decode_tma_kernel<T, KV8, D, false>;
+  static DeviceFlags attr, attr_f;
+  cudaError_t e = (merge_slots > 0 ? attr_f : attr).once([&] {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int grid = sms > 0 ? sms : 148;  // persistent: one CTA per SM
-  if (total_items < grid * C::W) grid = (total_items + C::W - 1) / C::W;
-  if (grid < 1) grid = 1;
-  k<<<grid, C::W * 32, C::SMEM, st>>>(a, tk, tv, total_items, n_mblk, counters);
+  const int grid = dec_grid<D, KV8>(total_items, sms);
+  k<<<grid, C::W * 32, C::SMEM, st>>>(a, tk, tv, total_items, n_mblk, counters, merge_slots);
   return cudaGetLastError();
 }
 
 template <typename T, bool KV8>
 cudaError_t launch_dec_d(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                         int items, int n_mblk, uint32_t* cnt, cudaStream_t st) {
+                         int items, int n_mblk, uint32_t* cnt, int merge_slots, int sms,
+                         cudaStream_t st) {
   switch (a.p.d) {
     case 64:
-      if constexpr (!KV8) return launch_dec<T, KV8, 64>(a, tk, tv, items, n_mblk, cnt, st);
+      if constexpr (!KV8)
+        return launch_dec<T, KV8, 64>(a, tk, tv, items, n_mblk, cnt, merge_slots, sms, st);
       break;
-    case 128: return launch_dec<T, KV8, 128>(a, tk, tv, items, n_mblk, cnt, st);
-    case 256: return launch_dec<T, KV8, 256>(a, tk, tv, items, n_mblk, cnt, st);
+    case 128: return launch_dec<T, KV8, 128>(a, tk, tv, items, n_mblk, cnt, merge_slots, sms, st);
+    case 256: return launch_dec<T, KV8, 256>(a, tk, tv, items, n_mblk, cnt, merge_slots, sms, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -667,8 +742,15 @@ bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens
   return kv_dtype == PA_E5M2 && (d == 128 || d == 256);
 }
 
+int decode_tma_grid(int d, bool kv8, int64_t items, int sms) {
+  const int n = items >= (int64_t(1) << 31) ? INT32_MAX : (int)items;
+  if (kv8) return d == 128 ? dec_grid<128, true>(n, sms) : dec_grid<256, true>(n, sms);
+  return d == 64 ? dec_grid<64, false>(n, sms)
+                 : d == 128 ? dec_grid<128, false>(n, sms) : dec_grid<256, false>(n, sms);
+}
+
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
-                              int n_units, cudaStream_t st) {
+                              int n_units, int merge_slots, int sms, cudaStream_t st) {
   if (a.p.num_rows == 0 || n_mblk == 0 || n_units <= 0) return cudaSuccess;
   const int64_t items = (int64_t)n_units * a.p.hkv * NSPLIT * n_mblk;
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
@@ -679,11 +761,12 @@ cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int 
     return cudaErrorInvalidValue;
   uint32_t* counters = reinterpret_cast<WsHeader*>(a.p.err)->pad;
   const bool kv8 = kv_dtype == PA_E5M2;
+  const int it = (int)items, ms = merge_slots;
   if (q_dtype == PA_BF16)
-    return kv8 ? launch_dec_d<__nv_bfloat16, true>(a, tk, tv, (int)items, n_mblk, counters, st)
-               : launch_dec_d<__nv_bfloat16, false>(a, tk, tv, (int)items, n_mblk, counters, st);
-  return kv8 ? launch_dec_d<__half, true>(a, tk, tv, (int)items, n_mblk, counters, st)
-             : launch_dec_d<__half, false>(a, tk, tv, (int)items, n_mblk, counters, st);
+    return kv8 ? launch_dec_d<__nv_bfloat16, true>(a, tk, tv, it, n_mblk, counters, ms, sms, st)
+               : launch_dec_d<__nv_bfloat16, false>(a, tk, tv, it, n_mblk, counters, ms, sms, st);
+  return kv8 ? launch_dec_d<__half, true>(a, tk, tv, it, n_mblk, counters, ms, sms, st)
+             : launch_dec_d<__half, false>(a, tk, tv, it, n_mblk, counters, ms, sms, st);
 }
 
 }  // namespace pa

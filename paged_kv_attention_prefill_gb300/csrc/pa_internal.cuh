@@ -204,9 +204,13 @@ cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int
                                cudaStream_t st);
 // persistent TMA-fed split-KV decode (16-bit q; same-type or fp8 E5M2 cache)
 bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
-// n_units: rows (packed) or decode slots (tokenwise) the work items range over
+// n_units: rows (packed) or decode slots (tokenwise) the work items range over;
+// merge_slots > 0: the kernel also merges the partial states of that many
+// decode slots itself (no merge kernel); sms: the device's SM count
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
-                              int n_units, cudaStream_t st);
+                              int n_units, int merge_slots, int sms, cudaStream_t st);
+// CTAs of that launch (one per SM at most)
+int decode_tma_grid(int d, bool kv8, int64_t items, int sms);
 bool decode_mma_supported(int q_dtype, int kv_dtype, int d);
 // Long-row decode (PA_SPLITS_BY_LENGTH): the list of work items of the rows
 // longer than LONG_MIN_TILES decode tiles, then their splits on the tcgen05
@@ -320,6 +324,64 @@ __device__ __forceinline__ void e5m2x4_to<__nv_bfloat16>(uint32_t w, uint32_t& l
   float2 fa = __half22float2(a), fb = __half22float2(b);
   lo = pack2<__nv_bfloat16>(fa.x, fa.y);
   hi = pack2<__nv_bfloat16>(fb.x, fb.y);
+}
+
+// Row of global query token t: the largest b with cu_q[b] <= t.
+__device__ __forceinline__ int row_of_token(const Problem& p, int t) {
+  int lo = 0, hi = p.num_rows - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Splits of the partition a decode token's partial states come from: those
+// of its row's length (of the token's own prefix for one-token verify rows).
+__device__ __forceinline__ int merge_splits(const AttnArgs& a, int t) {
+  const Problem& p = a.p;
+  const int b = row_of_token(p, t);
+  int L = __ldg(p.seq_lens + b);
+  if (a.tokenwise) {
+    const int qs = __ldg(p.cu_q + b), qb = __ldg(p.cu_q + b + 1) - qs;
+    L = L - qb + 1 + (t - qs);
+  }
+  return dec_num_splits(L, a.by_len);
+}
+
+// The split-KV merge of one (token, head) for NC columns (vllm-rlt PR #128,
+// "Purpose", decode: the partial softmax states combined by log-sum-exp):
+// M = max_k m_k over the splits k < nsp with l_k > 0, w_k = 2^(m_k - M),
+// res = (sum_k w_k acc_k) / (sum_k w_k l_k) * v_scale, summed in the fixed
+// order k = 0..15, so a row's result never depends on the batch; 0 when no
+// split saw a key.  Both the merge kernel and the decode kernel's
+// same-launch merge use it, so their results are the same bits.
+template <int NC>
+__device__ __forceinline__ void merge16(const float2 (&ml)[NSPLIT], const float (&acc)[NC][NSPLIT],
+                                        int nsp, float v_scale, float (&res)[NC]) {
+  float mstar = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k)
+    if (k < nsp && ml[k].y > 0.f) mstar = fmaxf(mstar, ml[k].x);
+  float w[NSPLIT];
+  float lsum = 0.f;
+#pragma unroll
+  for (int k = 0; k < NSPLIT; ++k) {
+    w[k] = 0.f;
+    if (k < nsp && ml[k].y > 0.f) {
+      w[k] = exp2f(ml[k].x - mstar);
+      lsum += w[k] * ml[k].y;
+    }
+  }
+  const float inv = lsum > 0.f ? v_scale / lsum : 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NSPLIT; ++k)
+      if (w[k] != 0.f) s += w[k] * acc[c][k];
+    res[c] = s * inv;
+  }
 }
 
 // Physical element offset of key j of row b, KV head kh, or -1 if the block

@@ -135,6 +135,8 @@ def test_rejects_bad_params(lib, name):
         (params(q_dtype=pa.PA_F32, kv_dtype=pa.PA_E5M2), UNSUPPORTED),
         (params(q_dtype=pa.PA_BF16, kv_dtype=pa.PA_F16), UNSUPPORTED),
         (params(num_splits=8), UNSUPPORTED),
+        (params(merge_mode=3), INVALID),
+        (params(merge_mode=-1), INVALID),
         (params(softmax_scale=float("nan")), INVALID),
     ]
     for p, want in cases:
