@@ -69,7 +69,6 @@ struct Resolved {
   int host_slots;     // decode slots (host mirrors)
   bool tc;            // prefill on the tcgen05 kernel
   bool tc2;           // prefill on the two-tile tcgen05 kernel
-  bool pair;          // ... on its CTA-pair form (same work items)
   int pf_bm;          // query rows per prefill work item
   int pf_parts;       // prefill parts the workspace holds (prefill_kv_parts, 4 for auto)
   bool pf_auto;       // part count chosen per call
@@ -237,8 +236,6 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
 
   const int64_t cache_tokens = (int64_t)bat->num_pages * r->P;
   r->tc2 = prefill_tc2_supported(r->qd, r->kvd, r->d, cache_tokens);
-  // the CTA-pair form measured slower than the two-tile kernel: not routed
-  r->pair = false && r->tc2 && prefill_pair_supported(r->qd, r->kvd, r->d, cache_tokens);
   r->tc = !r->tc2 && prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens);
   // one-token verify rows run on the TMA decode kernel only
   if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
@@ -456,9 +453,7 @@ cudaError_t run_prefill(const AttnArgs& a, const Resolved& r, int grid_tiles, in
                         cudaStream_t st) {
   if (r.qd == PA_F32) return launch_f32(a, 0, grid_tiles, 0, st);
   cudaError_t e;
-  if (r.pair)
-    e = launch_prefill_pair(a, r.qd, grid_tiles, st);
-  else if (r.tc2)
+  if (r.tc2)
     e = launch_prefill_tc2(a, r.qd, r.kvd, grid_tiles, st);
   else if (r.tc)
     e = launch_prefill_tc(a, r.qd, r.kvd, grid_tiles, st);

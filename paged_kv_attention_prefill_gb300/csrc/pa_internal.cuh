@@ -202,11 +202,6 @@ constexpr int PF_BM_TC2 = 256;
 bool prefill_tc2_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
 cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int grid_x,
                                cudaStream_t st);
-// tcgen05 prefill on CTA pairs (M = 256 MMAs over two SMs, each holding half
-// of every K / V tile): 16-bit Q with a same-type cache at d = 128; the same
-// 256-row work items as the two-tile kernel
-bool prefill_pair_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
-cudaError_t launch_prefill_pair(const AttnArgs& a, int q_dtype, int grid_x, cudaStream_t st);
 // persistent TMA-fed split-KV decode (16-bit q; same-type or fp8 E5M2 cache)
 bool decode_tma_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens);
 // n_units: rows (packed) or decode slots (tokenwise) the work items range over;

@@ -96,50 +96,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// One poll with acquire at cluster scope (for barriers that receive arrivals
-// from the other CTA of a pair).
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-#ifdef PA_WAIT_POLL_ONLY
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-#else
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-#endif
-  return ok != 0;
-}
-
-// mbar_wait for a CTA of a pair: acquire at cluster scope, and a wait that
-// runs out also raises the other CTA's abort flag (`peer_abort`, a
-// shared::cluster address), so both CTAs leave their waits at once.
-__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                             uint32_t peer_abort, uint32_t* err) {
-  if (mbar_try_wait_cl(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    if ((it & WAIT_CHECK_MASK) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-        *abort_flag = 1;
-        asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;\n" ::"r"(peer_abort), "r"(1)
-                     : "memory");
-        atomicOr(err, PA_DEVERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 // Bounded wait that ignores the abort flag: used to drain work the calling
 // thread itself started (copies, MMAs) before its resources go away.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint32_t* err) {
@@ -220,72 +176,6 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// CTA pairs (a cluster of two CTAs sharing one tcgen05 MMA of M = 256): the
-// pair's TMEM is allocated by one warp of each CTA together and holds the
-// same columns in both; MMAs are issued by one thread of rank 0; A is split
-// by rows (each CTA 128, from its own TMEM or shared memory at the same
-// offset) and B along N (each CTA N / 2 rows at the same shared offset); each
-// CTA's TMEM receives its 128 rows of D.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-// Whole-cluster barrier (every thread of both CTAs); release / acquire.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n"
-               ::: "memory");
-}
-// The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Arrival on an mbarrier given by its shared::cluster address (release at
-// cluster scope: this thread's earlier writes are visible to the waiter).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-// Arrives on `bar` (the same shared offset) in both CTAs of the pair once
-// every tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n" ::"r"(bar), "h"((uint16_t)3)
-      : "memory");
-}
-// The same, arriving on the issuing CTA's barrier only.
-__device__ __forceinline__ void tc_commit_pair_self(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-                   bar)
-               : "memory");
-}
-// M = 256 pair MMA, 16-bit inputs, fp32 accumulate, A from TMEM.
-__device__ __forceinline__ void tc_mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
