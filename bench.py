@@ -51,10 +51,10 @@ L2_BYTES = 129 * 1024 * 1024
 # only while the kernel's sources hash to the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "83c1a930af3249858d381673482eb0e52f79bdc9d5646544c1e70a5f9ce38ad8",
-        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "48ad9f70924798a53f893583c129da78740890cf13b315a2146acf9decea007b",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "4a8ce1425acea05a265752529ad3b1aa041b35f7c8354661bf286eded8e9dc2b",
+        "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "629b7fbaf3806ae668af86f08a63be4db05820bfc0a147133c0a08a4cf9fb924",
     },
-    "bytes_per_launch": 966179072 + 53469952,
+    "bytes_per_launch": 966678784 + 53437184,
 }
 
 
@@ -275,6 +275,22 @@ def part_mixed3(steps, warmup, stream, pk):
     res["whole_call_by_length"] = {"ms": round(lms, 4),
                                    "TFLOP/s_of_prefill": round(F / (lms * 1e-3) / 1e12, 1)}
     del lws
+    # and with the prefill row cut into key-range parts, the count chosen per
+    # call (the chunk's row is cut in 3)
+    aws = pa.make_workspace(pa.make_params(b.q, b.k_cache, num_splits=pa.PA_SPLITS_BY_LENGTH,
+                                           prefill_kv_parts=pa.PA_PREFILL_PARTS_AUTO),
+                            b.num_rows, b.total_q, "cuda")
+
+    def afn():
+        pa.paged_attn_mixed(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                            b.seq_lens, out=out, workspace=aws,
+                            num_splits=pa.PA_SPLITS_BY_LENGTH,
+                            prefill_kv_parts=pa.PA_PREFILL_PARTS_AUTO, **kw)
+    ams = time_calls(afn, steps, warmup, stream)
+    res["whole_call_by_length_auto_parts"] = {
+        "ms": round(ams, 4), "TFLOP/s_of_prefill": round(F / (ams * 1e-3) / 1e12, 1),
+        "note": "num_splits = PA_SPLITS_BY_LENGTH and prefill_kv_parts = PA_PREFILL_PARTS_AUTO"}
+    del aws
     # each half as a call of its own: the chunk's row through the prefill
     # entry, the three resident rows through the decode entry
     for name, rows, entry in (("prefill_row_alone", [0], pa.paged_attn_prefill),

@@ -290,9 +290,11 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
       }
     }
     // a part count chosen per call: only without decode rows, which run
-    // beside the prefill on the same SMs and take a share the count
-    // cannot see
-    if (r->pf_auto && (r->tc2 || r->tc) && entry != E_DECODE && r->host_slots == 0) {
+    // beside the prefill on the same SMs and take a share the count cannot
+    // see -- unless those rows' long splits run as short tile-kernel items
+    // (PA_SPLITS_BY_LENGTH), where the decode rows take a small share
+    if (r->pf_auto && (r->tc2 || r->tc) && entry != E_DECODE &&
+        (r->host_slots == 0 || r->long_tc)) {
       const int K = choose_parts(k_ends, r->hkv, sm_count());
       r->pf_cut = K > 1 ? K : 0;
       r->pf_min_units = PF_AUTO_UNITS;

@@ -45,15 +45,15 @@ def batch(q_lens=Q_LENS, kv_lens=KV_LENS, *, d=128, dtype="bf16", kv=None, P=16,
     return cpu, cpu.to("cuda")
 
 
-def run(entry, b, parts, host=True):
+def run(entry, b, parts, host=True, num_splits=0):
     extra = {}
     if host:
         extra = dict(cu_seqlens_q_host=b.cu_seqlens_q.cpu(), seq_lens_host=b.seq_lens.cpu())
-    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache, prefill_kv_parts=parts), b.num_rows,
-                           b.total_q, "cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache, prefill_kv_parts=parts,
+                                          num_splits=num_splits), b.num_rows, b.total_q, "cuda")
     out = ENTRY[entry](b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens,
                        softmax_scale=b.softmax_scale, k_scale=b.k_scale, v_scale=b.v_scale,
-                       prefill_kv_parts=parts, workspace=ws, **extra)
+                       prefill_kv_parts=parts, num_splits=num_splits, workspace=ws, **extra)
     torch.cuda.synchronize()
     assert pa.read_errors(ws) == 0
     return out
@@ -186,6 +186,12 @@ def test_auto_part_count_on_the_long_chunk():
     # nothing is cut
     assert bitwise(_run_auto("mixed", gpu), run("mixed", gpu, parts=0))
     assert bitwise(_run_auto("prefill", row, host=False), run("prefill", row, parts=0))
+    # unless the decode rows' long splits are short tile-kernel items
+    # (PA_SPLITS_BY_LENGTH): then the chunk is cut in 3 there too
+    by_len = pa.PA_SPLITS_BY_LENGTH
+    mixed = run("mixed", gpu, parts=pa.PA_PREFILL_PARTS_AUTO, num_splits=by_len)
+    assert bitwise(mixed, run("mixed", gpu, parts=3, num_splits=by_len))
+    assert bitwise(mixed[:2048], auto)
     del gpu, row
     torch.cuda.empty_cache()
 
