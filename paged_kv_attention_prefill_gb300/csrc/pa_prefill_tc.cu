@@ -563,8 +563,9 @@ __global__ void __launch_bounds__(384, 1)
 // fp8 E5M2 caches at d = 256: Q in TMEM and 128-key S tiles as above, but P
 // stays over S in TMEM (its 32 KB of shared memory go to the code rings), so
 // S(j) waits for the previous P V product.  The codes are streamed by TMA
-// into their own rings and widened by a fourth warpgroup (warps 12-15;
-// warps 2 and 3 idle) into the 16-bit tiles the MMAs read: an E5M2 code is
+// into their own rings (warp 0 the K codes, warp 2 the V codes, each ring
+// requested as soon as its stage is free; warp 3 idle) and widened by a
+// fourth warpgroup (warps 12-15) into the 16-bit tiles the MMAs read: an E5M2 code is
 // the high byte of the binary16 of the same value, and for bf16 Q it is
 // widened through fp32, also exactly.  Shared memory: 16-bit K 64 KB (one
 // tile), 16-bit V 2 x 32 KB (the two halves of a tile), K codes 2 x 32 KB,
@@ -690,17 +691,18 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ===== warp 0 streams the codes of each key tile: K (128 keys), then V ==
-    // in two 64-key halves, into the code rings: one TMA box (16 keys x 128
-    // codes) per page slot and 128-code chunk of the row; the slot holding
-    // the row's last key is copied by hand, zero-filled past the row's end.
-    const uint8_t* kc8 = static_cast<const uint8_t*>(a.kc);
-    const uint8_t* vc8 = static_cast<const uint8_t*>(a.vc);
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-    }
+  if (warp == 0 || warp == 2) {
+    // ===== warp 0 streams the K codes of each key tile (128 keys), warp 2 ==
+    // the V codes in 64-key halves, into the code rings: one TMA box (16
+    // keys x 128 codes) per page slot and 128-code chunk of the row; the slot
+    // holding the row's last key is copied by hand, zero-filled past the
+    // row's end.  Two warps, so that a ring waiting for its stage to be
+    // widened never holds back the other ring's requests (the codes take
+    // thousands of cycles to arrive).
+    const bool isK = warp == 0;
+    const uint8_t* cache8 = static_cast<const uint8_t*>(isK ? a.kc : a.vc);
+    const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+    if (lane == 0) tma_prefetch_desc(tmap);
     const int P = p.page_size;
     const int64_t bt_row = (int64_t)b * p.max_pages;
     // `rows` keys from kbase into the [chunk][rows][128 B] code tile dst
@@ -753,34 +755,25 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
           tma_load_3d(dst + c8 * (rows * 128) + lane * 16 * 128, tmap, c8 * 128, kh, tok0, fb);
       }
     };
+    // units: K tiles of BN keys (warp 0) or V halves of HB keys (warp 2)
+    const int n_units = isK ? n_tiles : 2 * n_tiles;
+    const int UK = isK ? C::BN : C::HB;
+    const uint32_t ring = isK ? sK8 : sV8, UB = isK ? C::K8_BYTES : C::V8_BYTES;
+    const int B_FULL = isK ? C::B_K8F : C::B_V8F, B_EMPTY = isK ? C::B_K8E : C::B_V8E;
     bool ok = true;
-    int nk = 0, nv = 0;  // K / V code units started
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j >= C::S8) ok = mbar_wait(bar(C::B_K8E + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, p.err);
+    int u = 0;  // units started
+    for (; u < n_units; ++u) {
+      if (u >= C::S8) ok = mbar_wait(bar(B_EMPTY + (u & 1)), ((u >> 1) - 1) & 1, abort_flag, p.err);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
-      unit(&tmK, kc8, k0 + j * C::BN, C::BN, sK8 + (j & 1) * C::K8_BYTES, bar(C::B_K8F + (j & 1)));
-      ++nk;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int q = 2 * j + h;
-        if (q >= C::S8) ok = mbar_wait(bar(C::B_V8E + (q & 1)), ((q >> 1) - 1) & 1, abort_flag, p.err);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        unit(&tmV, vc8, k0 + q * C::HB, C::HB, sV8 + (q & 1) * C::V8_BYTES, bar(C::B_V8F + (q & 1)));
-        ++nv;
-      }
+      unit(tmap, cache8, k0 + u * UK, UK, ring + (u & 1) * UB, bar(B_FULL + (u & 1)));
     }
     if (!ok) {
       // copies this warp started may still be landing: wait for them
-      for (int u = max(0, nk - C::S8); u < nk; ++u)
-        mbar_drain(bar(C::B_K8F + (u & 1)), (u >> 1) & 1, p.err);
-      for (int u = max(0, nv - C::S8); u < nv; ++u)
-        mbar_drain(bar(C::B_V8F + (u & 1)), (u >> 1) & 1, p.err);
+      for (int uu = max(0, u - C::S8); uu < u; ++uu)
+        mbar_drain(bar(B_FULL + (uu & 1)), (uu >> 1) & 1, p.err);
     }
   } else if (warp >= 12) {
     // ===== warps 12-15 widen every K tile (32 keys each) and V half (16 =====
