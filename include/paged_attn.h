@@ -145,7 +145,11 @@ typedef struct pa_params {
  * GPU (small batches, where the second launch costs more than the merge),
  * otherwise separate.  The result is the same bits either way.  Applies to
  * the TMA decode kernel (16-bit q) without PA_SPLITS_BY_LENGTH; other
- * decode paths, and the mixed call, always merge in a separate kernel.
+ * decode paths, and the mixed call, always merge in a separate kernel.  The
+ * same-launch merge needs every CTA of the decode grid resident at once: on
+ * a device whose SMs are partitioned between contexts (fewer SMs available
+ * than the device has), choose PA_MERGE_SEPARATE -- otherwise the barrier
+ * can only end by running out (PA_DEVERR_TIMEOUT, the merge skipped).
  */
 enum { PA_MERGE_AUTO = 0, PA_MERGE_SEPARATE = 1, PA_MERGE_SAME_LAUNCH = 2 };
 

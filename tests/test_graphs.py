@@ -97,3 +97,42 @@ def test_static_decode_capture_and_replay_bitwise():
                                      b.seq_lens, **kw)
         torch.cuda.synchronize()
         assert _bitwise(out_g, out_e)
+
+
+@pytest.mark.parametrize("entry", ["decode", "mixed"])
+def test_capture_and_replay_long_rows_split_by_length(entry):
+    # rows over 32768 keys cut into 2048-key parts on the tile kernel (its
+    # item list built on the device), with and without a prefill row beside
+    # them; replayed bitwise like the eager call, the merge in either place
+    q_lens = [1, 4, 1] if entry == "decode" else [200, 1, 4]
+    kv_lens = [40000, 36000, 900] if entry == "decode" else [3000, 40000, 36000]
+    b = workloads.make_batch(q_lens, kv_lens, num_q_heads=12, num_kv_heads=2, head_dim=256,
+                             page_size=16, q_dtype="f16", seed=53, device="cuda",
+                             data_device="cuda")
+    fn = {"mixed": pa.paged_attn_mixed, "decode": pa.paged_attn_decode}[entry]
+    by_len = pa.PA_SPLITS_BY_LENGTH
+    prm = pa.make_params(b.q, b.k_cache, num_splits=by_len)
+    for mode in (pa.PA_MERGE_SAME_LAUNCH, pa.PA_MERGE_SEPARATE):
+        ws = pa.make_workspace(prm, b.num_rows, b.total_q, "cuda")
+        ws_eager = pa.make_workspace(prm, b.num_rows, b.total_q, "cuda")
+        out_g = torch.empty_like(b.q)
+        kw = dict(_args(b), num_splits=by_len, merge_mode=mode)
+
+        def call(out, workspace):
+            fn(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens, out=out,
+               workspace=workspace, **kw)
+
+        call(out_g, ws)  # one-time set-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call(out_g, ws)
+        out_e = torch.empty_like(b.q)
+        for _ in range(3):
+            out_g.zero_()
+            g.replay()
+            call(out_e, ws_eager)
+            torch.cuda.synchronize()
+            assert _bitwise(out_g, out_e)
+        assert pa.read_errors(ws) == 0 and pa.read_errors(ws_eager) == 0
+        del g
