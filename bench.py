@@ -678,7 +678,9 @@ def run_reference(args):
     import oracle
     oracle.build()
     b = workloads.make_workload(HEADLINE_WORKLOAD, page_size=16)
-    budget = max(0.5, args.ref_seconds)
+    # each step one bounded sample, sized so that the whole run stays within
+    # about two and a half minutes whatever --steps and --warmup are
+    budget = min(args.ref_seconds, max(0.3, 150.0 / (args.steps + args.warmup)))
     vals, secs, descr, cores = [], [], "", oracle.num_threads()
     for s in range(args.warmup + args.steps):
         t = time.perf_counter()
