@@ -220,16 +220,20 @@ def graph_ms(fn, steps, warmup, stream):
     return ms
 
 
-def part_decode(n, steps, warmup, stream, pk):
+def part_decode(n, steps, warmup, stream, pk, by_length=False):
     import paged_kv_attention_prefill_gb300 as pa
     b = workloads.make_workload(n, device="cuda", data_device="cuda")
-    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache), b.num_rows, b.total_q, "cuda")
+    ws = pa.make_workspace(pa.make_params(b.q, b.k_cache, num_splits=pa.PA_SPLITS_BY_LENGTH),
+                           b.num_rows, b.total_q, "cuda")
     out = torch.empty_like(b.q)
     kw = call_args(b)
 
-    def fn():
-        pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
-                             b.seq_lens, out=out, workspace=ws, **kw)
+    def call(ns):
+        def fn():
+            pa.paged_attn_decode(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                                 b.seq_lens, out=out, workspace=ws, num_splits=ns, **kw)
+        return fn
+    fn = call(0)
     ms = time_calls(fn, steps, warmup, stream)
     ms_graph = graph_ms(fn, steps, warmup, stream)
     byt = metrics.decode_bytes(b.q_lens, b.kv_lens, num_q_heads=b.num_q_heads,
@@ -240,6 +244,12 @@ def part_decode(n, steps, warmup, stream, pk):
            "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
            "graph_replay_GB/s": round(byt / (ms_graph * 1e-3) / 1e9, 1),
            "launches_per_call": launches_per_call(b.q_lens, mixed=False)}
+    if by_length:
+        # the same batch with the length-only split count (2048-key parts)
+        ms_bl = time_calls(call(pa.PA_SPLITS_BY_LENGTH), steps, warmup, stream)
+        gbs_bl = byt / (ms_bl * 1e-3) / 1e9
+        res["by_length_splits"] = {"ms": round(ms_bl, 4), "GB/s": round(gbs_bl, 1),
+                                   "frac_of_hbm": round(gbs_bl / pk["hbm"], 4)}
     del b, ws, out
     torch.cuda.empty_cache()
     return res
@@ -634,7 +644,8 @@ def run_ours(args):
         if not args.headline_only:
             ps, pw = max(5, min(args.steps, 30)), 3
             parts["decode_split_kv_256rows"] = part_decode(4, ps, pw, stream, pk)
-            parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk)
+            parts["decode_long_context_fp8"] = part_decode(5, ps, pw, stream, pk,
+                                                           by_length=True)
             parts["mixed_chunk_plus_decode"] = part_mixed3(ps, pw, stream, pk)
             parts["prefill_fp8_cache"] = part_prefill_fp8(ps, pw, stream, pk)
             parts["prefill_fp8_cache_d256"] = part_prefill_fp8_d256(ps, pw, stream, pk)

@@ -213,15 +213,20 @@ enum { PA_PREFILL_PARTS_AUTO = -1 };
  * bits independent of the batch -- and its review thread leaves the count of
  * 16 untuned.  In this mode a row of at most 32768 keys keeps the 16 parts of
  * the default (bitwise the same result); a longer row is cut into parts of
- * 2048 keys (whole 64-key tiles), at most 128 of them (longer parts past
- * 262144 keys), and those parts run on the tcgen05 tile kernel with all of
- * the row's q_b * g GQA-packed query rows in one 128-row tile, so each part's
- * K/V is read once.  Still a function of the row's length alone: results
- * stay batch-invariant, page-size- and page-order-independent.  The partial
- * states take 128 slots per decode token and query head: the workspace is
- * sized for that (8x the default's partial-state bytes).  Built for head_dim
- * 256 with a 16-bit q and a same-type cache, packed verify rows; other
- * combinations return PA_ERR_UNSUPPORTED from the decode and mixed calls.
+ * 2048 keys (whole 128-key tiles), at most 128 of them (longer parts past
+ * 262144 keys).  At head_dim 256 with a 16-bit q and a same-type cache those
+ * parts run on the tcgen05 tile kernel with all of the row's q_b * g
+ * GQA-packed query rows in one 128-row tile, so each part's K/V is read
+ * once; otherwise on the decode kernel, whose many more, shorter work items
+ * then spread evenly over the GPU.  Still a function of the row's length
+ * alone: results stay batch-invariant, page-size- and page-order-independent.
+ * The partial states take 128 slots per decode token and query head: the
+ * workspace is sized for that (8x the default's partial-state bytes), and the
+ * merge always runs as a separate kernel.  Needs packed verify rows and a
+ * 16-bit q (the decode kernel's cases); fp32 and one-token verify rows return
+ * PA_ERR_UNSUPPORTED from the decode and mixed calls.  Without host mirrors
+ * the decode kernel walks 128 split indices per row and KV head (most of
+ * them empty for short rows).
  */
 enum { PA_SPLITS_BY_LENGTH = -1 };
 

@@ -76,6 +76,7 @@ struct Resolved {
   int pf_min_units;   // least 128-key units per part
   int by_len;         // length-only split count for long decode rows
   bool long_tc;       // long decode rows on the tcgen05 kernel
+  int split_cap;      // split indices per (row, KV head) on the decode kernel
   int host_long;      // long-row decode work items (host mirrors)
   int host_short;     // decode rows on the decode kernel (host mirrors)
   int merge_mode;     // PA_MERGE_*
@@ -240,15 +241,19 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   // one-token verify rows run on the TMA decode kernel only
   if (r->tokenwise && entry != E_PREFILL && !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
     return PA_ERR_UNSUPPORTED;
-  // length-only split counts for long rows: their splits run on the tcgen05
-  // tile kernel, built for d = 256 with 16-bit q and a same-type cache
+  // length-only split counts for long rows: the TMA decode kernel runs any
+  // count; the long rows' parts go to the tcgen05 tile kernel where it is
+  // built (d = 256, 16-bit q with a same-type cache)
   r->long_tc = false;
+  r->split_cap = NSPLIT;
   if (r->by_len && entry != E_PREFILL) {
-    if (r->tokenwise || r->d != 256 || r->kvd != r->qd ||
-        !prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens) ||
-        !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
+    if (r->tokenwise || !decode_tma_supported(r->qd, r->kvd, r->d, cache_tokens))
       return PA_ERR_UNSUPPORTED;
-    r->long_tc = true;
+    r->long_tc = r->d == 256 && r->kvd == r->qd &&
+                 prefill_tc_supported(r->qd, r->kvd, r->d, cache_tokens);
+    // without host mirrors the decode kernel's split indices cover the most
+    // parts a row can have (a tighter bound comes from the mirrors below)
+    if (!r->long_tc) r->split_cap = NSPLIT_MAX;
   }
   r->pf_bm = r->tc2 ? PF_BM_TC2 : r->tc ? PF_BM_TC : (r->qd == PA_F32 ? 16 : PF_BM);
   // an explicit part count applies as given; a count chosen per call needs
@@ -260,6 +265,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
   r->host_slots = 0;
   r->host_long = 0;
   r->host_short = 0;
+  int host_cap = 1;  // most parts of a row on the decode kernel
   if (r->host) {
     const int32_t* cu = bat->cu_seqlens_q_host;
     const int32_t* lens = bat->seq_lens_host;
@@ -277,10 +283,12 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
       if (dec) {
         r->host_max_q_dec = std::max(r->host_max_q_dec, qb);
         r->host_slots += qb;
-        if (r->long_tc && qb >= 1 && dec_is_long(L, 1))
+        if (r->long_tc && qb >= 1 && dec_is_long(L, 1)) {
           r->host_long += dec_num_splits(L, 1) * ((qb * r->g + LONG_BM - 1) / LONG_BM);
-        else if (qb >= 1)
+        } else if (qb >= 1) {
           ++r->host_short;
+          host_cap = std::max(host_cap, dec_num_splits(L, r->by_len));
+        }
       } else if (qb > 0) {
         const int nmb = (qb * r->g + bm - 1) / bm;
         for (int m = 0; m < nmb; ++m) {
@@ -289,6 +297,7 @@ pa_status validate(Entry entry, const pa_params* prm, const pa_batch* bat, const
         }
       }
     }
+    if (r->by_len && !r->long_tc) r->split_cap = host_cap;
     // a part count chosen per call: only without decode rows, which run
     // beside the prefill on the same SMs and take a share the count cannot
     // see -- unless those rows' long splits run as short tile-kernel items
@@ -349,7 +358,9 @@ AttnArgs make_args(const Resolved& r, const pa_batch* bat, const void* q, const 
   a.pf_ml = reinterpret_cast<float2*>(base + w.pf_ml);
   a.pf_acc = reinterpret_cast<float*>(base + w.pf_acc);
   a.split_stride = w.split_stride;
-  a.by_len = r.long_tc ? 1 : 0;
+  a.by_len = r.by_len;
+  a.long_tc = r.long_tc ? 1 : 0;
+  a.split_cap = r.split_cap;
   a.long_items = reinterpret_cast<const int2*>(base + w.long_items);
   a.n_long = &reinterpret_cast<const WsHeader*>(base)->n_long;
   a.max_long = w.max_long;
@@ -435,8 +446,8 @@ cudaError_t run_decode(const AttnArgs& a0, const Resolved& r, int n_mblk, int n_
     // decode grid leaves SMs idle, so the second launch would cost more
     const int sms = sm_count();
     int merge_slots = 0;
-    if (same_launch_ok && !r.long_tc && r.merge_mode != PA_MERGE_SEPARATE) {
-      const int64_t items = (int64_t)units * r.hkv * NSPLIT * n_mblk;
+    if (same_launch_ok && !r.by_len && r.merge_mode != PA_MERGE_SEPARATE) {
+      const int64_t items = (int64_t)units * r.hkv * a.split_cap * n_mblk;
       if (r.merge_mode == PA_MERGE_SAME_LAUNCH ||
           decode_tma_grid(r.d, r.kvd == PA_E5M2, items, sms) < sms)
         merge_slots = n_slots;

@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(1024) row_order_kernel(const AttnArgs a, int32
       if (dec) {
         const int L = max(p.seq_lens[i], 0);
         // rows on the long-row kernel take no decode-kernel items: last
-        work = a.by_len && dec_is_long(L, 1) ? 0u : (unsigned)dec_split_tiles(L, 0) + 1u;
+        work = a.long_tc && dec_is_long(L, 1) ? 0u : (unsigned)dec_split_tiles(L, a.by_len) + 1u;
       }
       key = ((unsigned long long)work << 32) | (unsigned)(n - i);
     }

@@ -131,8 +131,8 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
   const Problem& p = a.p;
   f.mblk = id % n_mblk;
   int rest = id / n_mblk;
-  f.split = rest % NSPLIT;
-  rest /= NSPLIT;
+  f.split = rest % a.split_cap;
+  rest /= a.split_cap;
   f.kh = rest % p.hkv;
   if (a.tokenwise) {
     // one-token rows: unit = decode slot; token i of row b is a row of its
@@ -173,13 +173,12 @@ __device__ __forceinline__ bool item_info(const AttnArgs& a, int id, int n_mblk,
       return false;
     }
     f.L = __ldg(p.seq_lens + f.b);
-    if (a.by_len && dec_is_long(f.L, 1)) return false;  // on the long-row kernel
+    if (a.long_tc && dec_is_long(f.L, 1)) return false;  // on the tile kernel
   }
   f.M = f.qb * p.g;
   f.r0 = f.mblk * 16;
   if (f.r0 >= f.M) return false;
-  const int n_tiles = (f.L + DEC_KT - 1) / DEC_KT;
-  const int tps = (n_tiles + NSPLIT - 1) / NSPLIT;
+  const int tps = dec_split_tiles(f.L, a.by_len);
   f.k0 = f.split * tps * DEC_KT;
   if (f.k0 >= f.L) return false;
   f.k1 = min(f.k0 + tps * DEC_KT, f.L);
@@ -752,7 +751,7 @@ int decode_tma_grid(int d, bool kv8, int64_t items, int sms) {
 cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int n_mblk,
                               int n_units, int merge_slots, int sms, cudaStream_t st) {
   if (a.p.num_rows == 0 || n_mblk == 0 || n_units <= 0) return cudaSuccess;
-  const int64_t items = (int64_t)n_units * a.p.hkv * NSPLIT * n_mblk;
+  const int64_t items = (int64_t)n_units * a.p.hkv * a.split_cap * n_mblk;
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;

@@ -167,6 +167,8 @@ struct AttnArgs {
   const uint32_t* n_slots;   // mixed: decode slots in use (device); null: every token is a slot
   int split_stride;          // partial states per (decode token, query head): 16 or NSPLIT_MAX
   int by_len;                // length-only split count for long rows (PA_SPLITS_BY_LENGTH)
+  int long_tc;               // ... whose parts run on the tile kernel (the decode kernel skips them)
+  int split_cap;             // split indices per (row or slot, KV head) on the decode kernel
   const int2* long_items;    // long-row decode items (row | m-block << 24, split)
   const uint32_t* n_long;    // their count (device)
   int64_t max_long;          // entries the list holds

@@ -81,16 +81,21 @@ def test_length_only_split_workspace_and_checks(lib):
     assert nlen - n16 <= 40 * (128 - 16) * per_split + items + 4 * 256
     assert lib.paged_attn_workspace_size(ctypes.byref(params(num_splits=-2)), 4, 4) == 0
     for name in ("paged_attn_decode", "paged_attn_mixed"):
-        # built for d = 256 with a 16-bit same-type cache and packed verify rows
-        for p in (params(num_splits=by_len),
-                  params(head_dim=256, q_dtype=pa.PA_F16, kv_dtype=pa.PA_E5M2,
+        # the decode kernel's cases (16-bit q) with packed verify rows
+        for p in (params(head_dim=256, q_dtype=pa.PA_F32, kv_dtype=pa.PA_F32,
                          num_splits=by_len),
-                  params(head_dim=256, q_dtype=pa.PA_F32, kv_dtype=pa.PA_F32,
+                  params(head_dim=64, q_dtype=pa.PA_F16, kv_dtype=pa.PA_E5M2,
                          num_splits=by_len),
                   params(head_dim=256, num_splits=by_len,
                          verify_mode=pa.PA_VERIFY_TOKENWISE)):
             assert FakeCall(lib, p, [1, 1], [10, 20])(name) == UNSUPPORTED
         assert FakeCall(lib, params(num_splits=-2), [1, 1], [10, 20])(name) == UNSUPPORTED
+        # the rest pass the argument checks (here they stop at the device)
+        for p in (params(num_splits=by_len),
+                  params(head_dim=256, q_dtype=pa.PA_F16, kv_dtype=pa.PA_E5M2,
+                         num_splits=by_len)):
+            rc = FakeCall(lib, p, [1, 1], [10, 20])(name)
+            assert rc in (OK, NO_DEVICE) if not torch.cuda.is_available() else True
 
 
 class FakeCall:

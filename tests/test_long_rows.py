@@ -4,11 +4,13 @@ oracle.
 
 A decode row of at most 32768 keys keeps the 16-part partition (bitwise the
 same result as the default); a longer row is cut into parts of 2048 keys
-(whole 64-key tiles) that run on the tcgen05 tile kernel, one 128-row tile
-holding all of the row's GQA-packed query rows.  The count depends on the
-row's length alone, so the invariances the pages require still hold bitwise:
-page size, physical page order, a row alone vs in a batch, the mixed call vs
-the decode call, with and without host mirrors.
+(whole 128-key tiles).  At d = 256 with a 16-bit cache the parts run on the
+tcgen05 tile kernel, one 128-row tile holding all of the row's GQA-packed
+query rows; with an fp8 cache or another head dim they run on the decode
+kernel.  The count depends on the row's length alone, so the invariances the
+pages require still hold bitwise: page size, physical page order, a row alone
+vs in a batch, the mixed call vs the decode call, with and without host
+mirrors.
 """
 import numpy as np
 import pytest
@@ -55,8 +57,8 @@ def same_bits(a, b):
     return torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def batch(q_lens, kv_lens, dtype="f16", P=16, hq=12, hkv=2, seed=0, **kw):
-    return workloads.make_batch(q_lens, kv_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=256,
+def batch(q_lens, kv_lens, dtype="f16", P=16, hq=12, hkv=2, seed=0, d=256, **kw):
+    return workloads.make_batch(q_lens, kv_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                                 page_size=P, q_dtype=dtype, seed=seed, device="cuda",
                                 data_device="cuda", **kw)
 
@@ -159,3 +161,53 @@ def test_workload3_decode_rows_by_length():
         del b
         torch.cuda.empty_cache()
     assert same_bits(outs[896], outs[784])
+
+
+# the decode kernel's cases: an fp8 cache (d = 256 and 128) and 16-bit caches
+# at d = 64 and 128
+DEC_CASES = {
+    "e5m2_d256": dict(dtype="f16", d=256, kv_dtype="e5m2", k_scale=0.5, v_scale=2.0),
+    "e5m2_d128": dict(dtype="bf16", d=128, kv_dtype="e5m2", k_scale=0.37, v_scale=1.7),
+    "bf16_d128": dict(dtype="bf16", d=128, hq=8),
+    "f16_d64": dict(dtype="f16", d=64, hq=8),
+}
+
+
+@pytest.mark.parametrize("case", list(DEC_CASES))
+def test_long_rows_on_the_decode_kernel(case):
+    kw = dict(DEC_CASES[case])
+    tol = 2e-2 if kw.get("kv_dtype") else 1e-2
+    b = batch(Q_LENS, KV_LENS, seed=45, **kw)
+    out = run("decode", b, num_splits=BY_LEN)
+    ref = oracle.paged_attention(**b.oracle_args())
+    assert max_err(out, ref) <= tol
+    # rows of at most 32768 keys: bitwise the default partition's result
+    dflt = run("decode", b)
+    cu = np.cumsum([0] + Q_LENS)
+    for r, L in enumerate(KV_LENS):
+        if L <= 32768:
+            assert same_bits(out[cu[r]:cu[r + 1]], dflt[cu[r]:cu[r + 1]]), r
+    # without host mirrors (128 split indices per row), the mixed call
+    assert same_bits(run("decode", b, host=False, num_splits=BY_LEN), out)
+    assert same_bits(run("mixed", b, num_splits=BY_LEN), out)
+    assert same_bits(run("mixed", b, host=False, num_splits=BY_LEN), out)
+    # page size and page order, and each long row alone
+    o = run("decode", batch(Q_LENS, KV_LENS, P=800, seed=45, perm_seed=5, **kw),
+            num_splits=BY_LEN)
+    assert same_bits(o, out)
+    for r in (1, 5):
+        alone = run("decode", workloads.sub_batch(b, [r], device="cuda"), num_splits=BY_LEN)
+        assert same_bits(alone, out[cu[r]:cu[r + 1]]), r
+
+
+def test_workload5_by_length_sampled():
+    # the long-context fp8 workload (64 rows of 128000-240000 keys) whole,
+    # sampled tokens against the oracle, and bitwise without host mirrors
+    b = workloads.make_workload(5, device="cuda", data_device="cuda")
+    out = run("decode", b, num_splits=BY_LEN)
+    toks = [0, 1, b.total_q // 2, b.total_q - 1]
+    ref = oracle.paged_attention(tokens=toks, **b.oracle_args())
+    assert max_err(out[toks], ref) <= 2e-2
+    assert same_bits(run("decode", b, host=False, num_splits=BY_LEN), out)
+    del b
+    torch.cuda.empty_cache()
