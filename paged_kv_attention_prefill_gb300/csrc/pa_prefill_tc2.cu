@@ -532,25 +532,37 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       // S_t(j) was issued after O_t += P_t(j-1) V completed, and its commit
       // covers every earlier MMA: O_t is stable here.
-      float x[C::BN];
+      // the row's logits as pairs (keys 2k, 2k + 1): the exponent argument
+      // and the row sum run on the paired fp32 instructions, each lane of
+      // which rounds as its scalar form does
+      float2 x[C::BN / 2];
       float mt;  // max raw logit of the row in this tile (masked keys -> -inf)
       {
         uint32_t u[C::BN];
         mt = tmem_ld_red_max_x128(trow, u);  // the load also returns the row's max
 #pragma unroll
-        for (int k = 0; k < C::BN; ++k) x[k] = __uint_as_float(u[k]);
+        for (int k = 0; k < C::BN / 2; ++k)
+          x[k] = make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
       }
       const int kb = j * C::BN;
       if (kb + C::BN - 1 > last) {
         // a tile on the row's diagonal: mask, and take the max of what is left
 #pragma unroll
-        for (int k = 0; k < C::BN; ++k)
-          if (kb + k > last) x[k] = -INFINITY;
+        for (int k = 0; k < C::BN / 2; ++k) {
+          if (kb + 2 * k > last) x[k].x = -INFINITY;
+          if (kb + 2 * k + 1 > last) x[k].y = -INFINITY;
+        }
         float pm[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+        for (int u = 0; u < 4; ++u) {
+          pm[2 * u] = x[u].x;
+          pm[2 * u + 1] = x[u].y;
+        }
 #pragma unroll
-        for (int k = 8; k < C::BN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        for (int k = 4; k < C::BN / 2; ++k) {
+          pm[2 * (k & 3)] = fmaxf(pm[2 * (k & 3)], x[k].x);
+          pm[2 * (k & 3) + 1] = fmaxf(pm[2 * (k & 3) + 1], x[k].y);
+        }
         mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
@@ -579,17 +591,23 @@ __global__ void __launch_bounds__(384, 1)
       }
       // P (16-bit pairs) over the first BN / 2 columns of S, in two halves of
       // 64 keys, each published as soon as it is in TMEM
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+      // partial row sums, fixed order: key k adds into sum k mod 8
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+      const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(nmu, nmu);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int k = 64 * h; k < 64 * h + 64; ++k) {
-          x[k] = ex2(fmaf(x[k], sl2, nmu));
-          ps[k & 7] += x[k];
+        for (int k = 32 * h; k < 32 * h + 32; ++k) {
+          float2 y = __ffma2_rn(x[k], sl2v, nmv);
+          y.x = ex2(y.x);
+          y.y = ex2(y.y);
+          x[k] = y;
+          ps[k & 3] = __fadd2_rn(ps[k & 3], y);
         }
         uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pk[k] = pack2<T>(x[64 * h + 2 * k], x[64 * h + 2 * k + 1]);
+        for (int k = 0; k < 32; ++k) pk[k] = pack2<T>(x[32 * h + k].x, x[32 * h + k].y);
         tmem_st_x32_nowait(trow + 32 * h, pk);
         tmem_wait_st();
         tc_fence_before();
@@ -597,7 +615,8 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar((h ? C::B_PF2 : C::B_PF) + t));
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const float rs = ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) +
+                       ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
       l = l * factor + rs;
     }
     // ---- epilogue: out = O / l * v_scale, or this part's (O, m, l) ----
