@@ -404,24 +404,35 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       // S(j) may run while the previous P V product still does: O and P's
       // buffer are touched only after waiting for that product
-      float x[HN];
+      // the logits as pairs (keys 2k, 2k + 1) for the paired fp32
+      // instructions below, each lane of which rounds as its scalar form does
+      float2 x[HN / 2];
       float mt;  // max raw logit of this half tile (masked keys -> -inf)
       {
         uint32_t u[HN];
         mt = tmem_ld_red_max_x64(trow + hf * HN, u);  // the load also returns the max
 #pragma unroll
-        for (int k = 0; k < HN; ++k) x[k] = __uint_as_float(u[k]);
+        for (int k = 0; k < HN / 2; ++k)
+          x[k] = make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
       }
       const int kb = j * C::BN + hf * HN;
       if (kb + HN - 1 > last) {
 #pragma unroll
-        for (int k = 0; k < HN; ++k)
-          if (kb + k > last) x[k] = -INFINITY;
+        for (int k = 0; k < HN / 2; ++k) {
+          if (kb + 2 * k > last) x[k].x = -INFINITY;
+          if (kb + 2 * k + 1 > last) x[k].y = -INFINITY;
+        }
         float pm[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+        for (int u = 0; u < 4; ++u) {
+          pm[2 * u] = x[u].x;
+          pm[2 * u + 1] = x[u].y;
+        }
 #pragma unroll
-        for (int k = 8; k < HN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        for (int k = 4; k < HN / 2; ++k) {
+          pm[2 * (k & 3)] = fmaxf(pm[2 * (k & 3)], x[k].x);
+          pm[2 * (k & 3) + 1] = fmaxf(pm[2 * (k & 3) + 1], x[k].y);
+        }
         mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
@@ -461,11 +472,19 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st_x32(trow + C::O_COL + hf * HD + c * 32, o);
         }
       }
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+      // partial row sums, fixed order: key k adds into sum k mod 8
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+      {
+        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(nmu, nmu);
 #pragma unroll
-      for (int k = 0; k < HN; ++k) {
-        x[k] = ex2(fmaf(x[k], sl2, nmu));
-        ps[k & 7] += x[k];
+        for (int k = 0; k < HN / 2; ++k) {
+          float2 y = __ffma2_rn(x[k], sl2v, nmv);
+          y.x = ex2(y.x);
+          y.y = ex2(y.y);
+          x[k] = y;
+          ps[k & 3] = __fadd2_rn(ps[k & 3], y);
+        }
       }
       {
         // P (16-bit) of this warpgroup's keys into half hf of P's buffer
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(384, 1)
         // previous tile's product has read that half; one arrival per warp
         uint32_t pk[HN / 2];
 #pragma unroll
-        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
+        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[k].x, x[k].y);
         if (j > 0) mbar_wait(bar(C::B_PV + hf), (j - 1) & 1, abort_flag, p.err);
         const uint32_t prow = sP + hf * (C::BM * 128) + r * 128;
 #pragma unroll
@@ -484,7 +503,8 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PF + hf));
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const float rs = ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) +
+                       ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
       l = l * factor + rs;
     }
     // ---- epilogue: out = O / (l_0 + l_1) * v_scale, or this part's state ----
@@ -924,24 +944,35 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
       mbar_wait(bar(C::B_SF), j & 1, abort_flag, p.err);
       tc_fence_after();
       // S(j) was issued after the previous P V product completed: O is stable
-      float x[HN];
+      // the logits as pairs (keys 2k, 2k + 1) for the paired fp32
+      // instructions below, each lane of which rounds as its scalar form does
+      float2 x[HN / 2];
       float mt;  // max raw logit of this half tile (masked keys -> -inf)
       {
         uint32_t u[HN];
         mt = tmem_ld_red_max_x64(trow + hf * HN, u);  // the load also returns the max
 #pragma unroll
-        for (int k = 0; k < HN; ++k) x[k] = __uint_as_float(u[k]);
+        for (int k = 0; k < HN / 2; ++k)
+          x[k] = make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
       }
       const int kb = j * C::BN + hf * HN;
       if (kb + HN - 1 > last) {
 #pragma unroll
-        for (int k = 0; k < HN; ++k)
-          if (kb + k > last) x[k] = -INFINITY;
+        for (int k = 0; k < HN / 2; ++k) {
+          if (kb + 2 * k > last) x[k].x = -INFINITY;
+          if (kb + 2 * k + 1 > last) x[k].y = -INFINITY;
+        }
         float pm[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pm[u] = x[u];
+        for (int u = 0; u < 4; ++u) {
+          pm[2 * u] = x[u].x;
+          pm[2 * u + 1] = x[u].y;
+        }
 #pragma unroll
-        for (int k = 8; k < HN; ++k) pm[k & 7] = fmaxf(pm[k & 7], x[k]);
+        for (int k = 4; k < HN / 2; ++k) {
+          pm[2 * (k & 3)] = fmaxf(pm[2 * (k & 3)], x[k].x);
+          pm[2 * (k & 3) + 1] = fmaxf(pm[2 * (k & 3) + 1], x[k].y);
+        }
         mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
@@ -974,24 +1005,33 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
           tmem_st_x32(trow + C::O_COL + hf * HD + c * 32, o);
         }
       }
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums, fixed order
+      // partial row sums, fixed order: key k adds into sum k mod 8
+      float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
+      {
+        const float2 sl2v = make_float2(sl2, sl2), nmv = make_float2(nmu, nmu);
 #pragma unroll
-      for (int k = 0; k < HN; ++k) {
-        x[k] = ex2(fmaf(x[k], sl2, nmu));
-        ps[k & 7] += x[k];
+        for (int k = 0; k < HN / 2; ++k) {
+          float2 y = __ffma2_rn(x[k], sl2v, nmv);
+          y.x = ex2(y.x);
+          y.y = ex2(y.y);
+          x[k] = y;
+          ps[k & 3] = __fadd2_rn(ps[k & 3], y);
+        }
       }
       {
         // P (16-bit pairs) over this warpgroup's keys: HN / 2 columns at the
         // start of S, then one arrival per warp
         uint32_t pk[HN / 2];
 #pragma unroll
-        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[2 * k], x[2 * k + 1]);
+        for (int k = 0; k < HN / 2; ++k) pk[k] = pack2<T>(x[k].x, x[k].y);
         tmem_st_x32(trow + hf * (HN / 2), pk);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_PF));
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const float rs = ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) +
+                       ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
       l = l * factor + rs;
     }
     // ---- epilogue: out = O / (l_0 + l_1) * v_scale, or this part's state ----
