@@ -197,9 +197,11 @@ enum { PA_VERIFY_PACKED = 0, PA_VERIFY_TOKENWISE = 1 };
  * count that takes the fewest full-CTA times); launches with four or more
  * waves, or whose longest item has fewer than 8192 keys, are not cut.  It
  * needs the host mirrors and applies to calls without decode rows, and to
- * mixed calls whose decode rows use num_splits = PA_SPLITS_BY_LENGTH (their
- * long splits are short items that take a small share of the SMs); other
- * mixed calls with decode rows, and calls without mirrors, are not cut.
+ * mixed calls whose decode rows use num_splits = PA_SPLITS_BY_LENGTH with
+ * their long parts on the tile kernel (head_dim 256, a 16-bit q and a
+ * same-type cache: those parts are short items that take a small share of
+ * the SMs); other mixed calls with decode rows, and calls without mirrors,
+ * are not cut.
  * The count depends on the whole batch, so a prefill row's bits may differ
  * between batches (still independent of the page size and the pages); the
  * workspace is sized for 4 parts.
