@@ -24,6 +24,11 @@
 //    straight from the block table (1Cat-vLLM PR #616, original description:
 //    any page size that is a multiple of 16); the slot holding the row's last
 //    key is copied by hand with the keys past the row's end zero-filled.
+//    With pages of at least 128 tokens (a kernel instance of its own), a
+//    unit whose slots are one run of one page takes one box per 128-byte
+//    chunk instead: the issue of one TMA request per slot and chunk, not the
+//    copies' flight time, was what held these kernels back (the mixed
+//    workload's chunk row, pages of 784 tokens: 6.83 -> 5.31 ms).
 //  * Warp 1, one thread, issues S(0), then per key tile j: S(j + 1) once the
 //    softmax has read S(j), and O += P(j) V in two 64-key halves, each once
 //    that half of P(j) is in shared memory.
@@ -83,10 +88,12 @@ struct TcCfg {
   static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
 };
 
-template <typename T, bool DEC>
+template <typename T, bool DEC, bool WIDE>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKw,
+                      const __grid_constant__ CUtensorMap tmVw) {
   using C = TcCfg;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
@@ -220,8 +227,14 @@ __global__ void __launch_bounds__(384, 1)
     const int B_FULL = isK ? C::B_KF : C::B_VF, B_EMPTY = isK ? C::B_KE : C::B_VE;
     const uint32_t ring = isK ? sK : sV;
     const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+    // the same view with one box per unit (UK rows), for units whose keys
+    // lie in one page
+    const void* tmapw = isK ? static_cast<const void*>(&tmKw) : static_cast<const void*>(&tmVw);
     const T* cache = static_cast<const T*>(isK ? a.kc : a.vc);
-    if (lane == 0) tma_prefetch_desc(tmap);
+    if (lane == 0) {
+      tma_prefetch_desc(tmap);
+      if (WIDE) tma_prefetch_desc(tmapw);
+    }
     const int P = p.page_size;
     const int64_t bt_row = (int64_t)b * p.max_pages;
     const int n_units = isK ? n_tiles : 2 * n_tiles;
@@ -254,6 +267,19 @@ __global__ void __launch_bounds__(384, 1)
             kind = (s0 + 16 <= L) ? 1 : 2;
           }
         }
+      }
+      const int tok_first = __shfl_sync(0xffffffffu, tok0, 0);
+      if (WIDE &&
+          __all_sync(0xffffffffu, lane >= slots || (kind == 1 && tok0 == tok_first + 16 * lane))) {
+        // every slot whole and in one run of one page: one box per chunk
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_FULL + st), (uint32_t)UK * D * 2u);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(dst + c * (UK * 128), tmapw, c * 64, kh, tok_first, bar(B_FULL + st));
+        }
+        __syncwarp();
+        continue;
       }
       uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
       while (manual) {
@@ -632,10 +658,12 @@ struct Tc8Cfg {
   static_assert(NBAR * 8 <= BAR_AREA, "barrier area");
 };
 
-template <typename T>
+template <typename T, bool WIDE>
 __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
     prefill_tc8_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmKw,
+                       const __grid_constant__ CUtensorMap tmVw) {
   using C = Tc8Cfg;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
@@ -722,12 +750,17 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
     const bool isK = warp == 0;
     const uint8_t* cache8 = static_cast<const uint8_t*>(isK ? a.kc : a.vc);
     const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
-    if (lane == 0) tma_prefetch_desc(tmap);
+    // the same view with one box per unit, for units whose keys lie in one page
+    const void* tmapw = isK ? static_cast<const void*>(&tmKw) : static_cast<const void*>(&tmVw);
+    if (lane == 0) {
+      tma_prefetch_desc(tmap);
+      if (WIDE) tma_prefetch_desc(tmapw);
+    }
     const int P = p.page_size;
     const int64_t bt_row = (int64_t)b * p.max_pages;
     // `rows` keys from kbase into the [chunk][rows][128 B] code tile dst
-    auto unit = [&](const void* tmap, const uint8_t* cache, int kbase, int rows, uint32_t dst,
-                    uint32_t fb) {
+    auto unit = [&](const void* tmap, const void* tmapw, const uint8_t* cache, int kbase, int rows,
+                    uint32_t dst, uint32_t fb) {
       // slot `lane`: 1 = whole slot by TMA, 2 = partial (by hand), 3 = zero-fill
       int kind = 0, tok0 = 0;
       if (lane < rows / 16) {
@@ -745,6 +778,19 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
             kind = (s0 + 16 <= L) ? 1 : 2;
           }
         }
+      }
+      const int tok_first = __shfl_sync(0xffffffffu, tok0, 0);
+      if (WIDE && __all_sync(0xffffffffu,
+                             lane >= rows / 16 || (kind == 1 && tok0 == tok_first + 16 * lane))) {
+        // every slot whole and in one run of one page: one box per chunk
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, (uint32_t)rows * (uint32_t)D);
+#pragma unroll
+          for (int c8 = 0; c8 < C::NC8; ++c8)
+            tma_load_3d(dst + c8 * (rows * 128), tmapw, c8 * 128, kh, tok_first, fb);
+        }
+        __syncwarp();
+        return;
       }
       uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
       while (manual) {
@@ -788,7 +834,7 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
         ok = false;
         break;
       }
-      unit(tmap, cache8, k0 + u * UK, UK, ring + (u & 1) * UB, bar(B_FULL + (u & 1)));
+      unit(tmap, tmapw, cache8, k0 + u * UK, UK, ring + (u & 1) * UB, bar(B_FULL + (u & 1)));
     }
     if (!ok) {
       // copies this warp started may still be landing: wait for them
@@ -1122,14 +1168,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 128 bytes
 // (64 16-bit elements or 128 fp8 codes), 128-byte swizzle.
-bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
-                   int64_t tokens) {
+bool encode_kv_map_rows(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                        int64_t tokens, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int elt = kv_dtype == PA_E5M2 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)d * elt, (cuuint64_t)hkv * d * elt};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), 1, 16};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / elt), 1, (cuuint32_t)rows};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt = kv_dtype == PA_E5M2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                  : kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -1139,19 +1185,38 @@ bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                   int64_t tokens) {
+  return encode_kv_map_rows(tm, cache, kv_dtype, d, hkv, tokens, 16);
+}
+
 namespace {
 
 template <typename T>
-cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
-                      bool kv8, cudaStream_t st) {
-  auto k = kv8 ? prefill_tc8_kernel<T> : prefill_tc_kernel<T, false>;
-  const uint32_t smem = kv8 ? Tc8Cfg::SMEM : TcCfg::SMEM;
-  static DeviceFlags attr16, attr8;
-  cudaError_t e = (kv8 ? attr8 : attr16).once([&] {
-    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t launch_tc(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap* tkw, const CUtensorMap* tvw, int grid_x, bool kv8,
+                      cudaStream_t st) {
+  // pages that can hold a whole key tile: the kernels that may copy a unit in
+  // one box per chunk
+  const bool wide = a.p.page_size >= TcCfg::BN;
+  if (kv8) {
+    auto k = wide ? prefill_tc8_kernel<T, true> : prefill_tc8_kernel<T, false>;
+    static DeviceFlags attr8, attr8w;
+    cudaError_t e = (wide ? attr8w : attr8).once([&] {
+      return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc8Cfg::SMEM);
+    });
+    if (e != cudaSuccess) return e;
+    k<<<dim3((unsigned)grid_x * a.p.hkv), Tc8Cfg::THREADS, Tc8Cfg::SMEM, st>>>(a, tk, tv, *tkw,
+                                                                              *tvw);
+    return cudaGetLastError();
+  }
+  auto k = wide ? prefill_tc_kernel<T, false, true> : prefill_tc_kernel<T, false, false>;
+  static DeviceFlags attr16, attr16w;
+  cudaError_t e = (wide ? attr16w : attr16).once([&] {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), kv8 ? Tc8Cfg::THREADS : 384, smem, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, TcCfg::SMEM, st>>>(a, tk, tv, *tkw, *tvw);
   return cudaGetLastError();
 }
 
@@ -1163,14 +1228,16 @@ namespace {
 // CTAs take the list's (item, KV head) units in turn).
 template <typename T>
 cudaError_t launch_tc_long(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
-                           int grid, cudaStream_t st) {
-  auto k = prefill_tc_kernel<T, true>;
-  static DeviceFlags attr;
-  cudaError_t e = attr.once([&] {
+                           const CUtensorMap& tkw, const CUtensorMap& tvw, int grid,
+                           cudaStream_t st) {
+  const bool wide = a.p.page_size >= TcCfg::BN;
+  auto k = wide ? prefill_tc_kernel<T, true, true> : prefill_tc_kernel<T, true, false>;
+  static DeviceFlags attr, attrw;
+  cudaError_t e = (wide ? attrw : attr).once([&] {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid), 384, TcCfg::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid), 384, TcCfg::SMEM, st>>>(a, tk, tv, tkw, tvw);
   return cudaGetLastError();
 }
 
@@ -1180,12 +1247,14 @@ cudaError_t launch_decode_long(const AttnArgs& a, int q_dtype, int grid, cudaStr
   if (grid <= 0) return cudaSuccess;
   if (a.p.d != 256) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tkw, tvw;
   if (!encode_kv_map(&tk, a.kc, q_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens))
+      !encode_kv_map(&tv, a.vc, q_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map_rows(&tkw, a.kc, q_dtype, a.p.d, a.p.hkv, tokens, TcCfg::BN) ||
+      !encode_kv_map_rows(&tvw, a.vc, q_dtype, a.p.d, a.p.hkv, tokens, TcCfg::HB))
     return cudaErrorInvalidValue;
-  return q_dtype == PA_BF16 ? launch_tc_long<__nv_bfloat16>(a, tk, tv, grid, st)
-                            : launch_tc_long<__half>(a, tk, tv, grid, st);
+  return q_dtype == PA_BF16 ? launch_tc_long<__nv_bfloat16>(a, tk, tv, tkw, tvw, grid, st)
+                            : launch_tc_long<__half>(a, tk, tv, tkw, tvw, grid, st);
 }
 
 bool prefill_tc_supported(int q_dtype, int kv_dtype, int d, int64_t cache_tokens) {
@@ -1198,13 +1267,18 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, int q_dtype, int kv_dtype, int 
   if (grid_x == 0) return cudaSuccess;
   if (a.p.d != 256) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tkw, tvw;
   if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
       !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
   const bool kv8 = kv_dtype == PA_E5M2;
-  return q_dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, tk, tv, grid_x, kv8, st)
-                            : launch_tc<__half>(a, tk, tv, grid_x, kv8, st);
+  // one box per K tile (BN keys) or V half (HB keys): the same in both kernels
+  static_assert(TcCfg::BN == Tc8Cfg::BN && TcCfg::HB == Tc8Cfg::HB, "unit sizes");
+  if (!encode_kv_map_rows(&tkw, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens, TcCfg::BN) ||
+      !encode_kv_map_rows(&tvw, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens, TcCfg::HB))
+    return cudaErrorInvalidValue;
+  return q_dtype == PA_BF16 ? launch_tc<__nv_bfloat16>(a, tk, tv, &tkw, &tvw, grid_x, kv8, st)
+                            : launch_tc<__half>(a, tk, tv, &tkw, &tvw, grid_x, kv8, st);
 }
 
 }  // namespace pa

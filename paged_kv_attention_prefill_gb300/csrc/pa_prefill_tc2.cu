@@ -14,6 +14,8 @@
 //    TMA box (1Cat-vLLM PR #616, original description: any page size that is
 //    a multiple of 16), into two shared-memory rings.  The slot that holds a
 //    row's last key is copied by hand with the keys past the end zero-filled.
+//    With pages of at least 128 tokens (the kernel's WIDE instance), a tile
+//    whose slots are one run of one page takes one box per 128-byte chunk.
 //  * Warp 1, one thread, issues tcgen05.mma for both query tiles in turn:
 //    S_t = Q_t K^T into tile t's S columns of TMEM, O_t += P_t V with P_t
 //    read from TMEM.  While one softmax warpgroup works on its S, the tensor
@@ -38,6 +40,8 @@
 namespace pa {
 bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
                    int64_t tokens);
+bool encode_kv_map_rows(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                        int64_t tokens, int rows);
 
 namespace {
 
@@ -98,10 +102,12 @@ struct Tc2Cfg {
   static_assert(!KV8 || D == 128, "fp8 caches: one 128-byte TMA box per key row");
 };
 
-template <typename T, int D, bool KV8>
+template <typename T, int D, bool KV8, bool WIDE>
 __global__ void __launch_bounds__(384, 1)
     prefill_tc2_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV) {
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmKw,
+                       const __grid_constant__ CUtensorMap tmVw) {
   using C = Tc2Cfg<D, KV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -206,6 +212,10 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) {
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (WIDE) {
+          tma_prefetch_desc(&tmKw);
+          tma_prefetch_desc(&tmVw);
+        }
       }
       const int P = p.page_size;
       const int64_t bt_row = (int64_t)b * p.max_pages;
@@ -234,6 +244,10 @@ __global__ void __launch_bounds__(384, 1)
         }
         const uint32_t manual_all = __ballot_sync(0xffffffffu, kind >= 2);
         const int n_tma = __popc(__ballot_sync(0xffffffffu, kind == 1));
+        // every slot whole and in one run of one page: one box per tile
+        const int tok_first = __shfl_sync(0xffffffffu, tok0, 0);
+        const bool whole = WIDE && __all_sync(0xffffffffu, lane >= C::SLOTS ||
+                                                                     (kind == 1 && tok0 == tok_first + 16 * lane));
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           if (j >= C::S8)
@@ -245,6 +259,16 @@ __global__ void __launch_bounds__(384, 1)
           }
           const uint32_t dst = (kv ? sV8 : sK8) + st * C::KV8_BYTES;
           const uint8_t* cache = kv ? vc8 : kc8;
+          if (whole) {
+            const uint32_t fb = bar((kv ? C::B_V8F : C::B_K8F) + st);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, (uint32_t)C::BN * 128u);
+              tma_load_3d(dst, kv ? (const void*)&tmVw : (const void*)&tmKw, 0, kh, tok_first, fb);
+            }
+            __syncwarp();
+            ++started[kv];
+            continue;
+          }
           uint32_t manual = manual_all;
           while (manual) {
             const int s = __ffs(manual) - 1;
@@ -336,8 +360,14 @@ __global__ void __launch_bounds__(384, 1)
       const int B_FULL = isK ? C::B_KF : C::B_VF, B_EMPTY = isK ? C::B_KE : C::B_VE;
       const uint32_t ring = isK ? sK : sV;
       const void* tmap = isK ? static_cast<const void*>(&tmK) : static_cast<const void*>(&tmV);
+      // the same view with one box per key tile, for tiles whose keys lie in
+      // one page
+      const void* tmapw = isK ? static_cast<const void*>(&tmKw) : static_cast<const void*>(&tmVw);
       const T* cache = static_cast<const T*>(isK ? a.kc : a.vc);
-      if (lane == 0) tma_prefetch_desc(tmap);
+      if (lane == 0) {
+        tma_prefetch_desc(tmap);
+        if (WIDE) tma_prefetch_desc(tmapw);
+      }
       const int P = p.page_size;
       const int64_t bt_row = (int64_t)b * p.max_pages;
       int j = 0;
@@ -368,6 +398,19 @@ __global__ void __launch_bounds__(384, 1)
               kind = (s0 + 16 <= L) ? 1 : 2;
             }
           }
+        }
+        const int tok_first = __shfl_sync(0xffffffffu, tok0, 0);
+        if (WIDE && __all_sync(0xffffffffu, lane >= C::SLOTS ||
+                                                      (kind == 1 && tok0 == tok_first + 16 * lane))) {
+          // every slot whole and in one run of one page: one box per chunk
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_FULL + st), (uint32_t)C::BN * D * 2u);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d(dst + c * (C::BN * 128), tmapw, c * 64, kh, tok_first, bar(B_FULL + st));
+          }
+          __syncwarp();
+          continue;
         }
         uint32_t manual = __ballot_sync(0xffffffffu, kind >= 2);
         while (manual) {
@@ -682,16 +725,19 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 template <typename T, int D, bool KV8>
-cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, int grid_x,
-                       cudaStream_t st) {
+cudaError_t launch_tc2(const AttnArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tkw, const CUtensorMap& tvw, int grid_x, cudaStream_t st) {
   using C = Tc2Cfg<D, KV8>;
-  auto k = prefill_tc2_kernel<T, D, KV8>;
-  static DeviceFlags attr;
-  cudaError_t e = attr.once([&] {
+  // pages that can hold a whole key tile: the kernel that may copy a tile in
+  // one box per chunk
+  const bool wide = a.p.page_size >= C::BN;
+  auto k = wide ? prefill_tc2_kernel<T, D, KV8, true> : prefill_tc2_kernel<T, D, KV8, false>;
+  static DeviceFlags attr, attr_w;
+  cudaError_t e = (wide ? attr_w : attr).once([&] {
     return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   });
   if (e != cudaSuccess) return e;
-  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, C::SMEM, st>>>(a, tk, tv);
+  k<<<dim3((unsigned)grid_x * a.p.hkv), 384, C::SMEM, st>>>(a, tk, tv, tkw, tvw);
   return cudaGetLastError();
 }
 
@@ -702,8 +748,10 @@ bool regs_ok() {
   static int ok = -1;
   if (ok < 0) {
     cudaFuncAttributes fa{};
-    ok = cudaFuncGetAttributes(&fa, prefill_tc2_kernel<T, D, KV8>) == cudaSuccess &&
-         fa.numRegs == REG_LAUNCH;
+    cudaFuncAttributes fw{};
+    ok = cudaFuncGetAttributes(&fa, prefill_tc2_kernel<T, D, KV8, false>) == cudaSuccess &&
+         cudaFuncGetAttributes(&fw, prefill_tc2_kernel<T, D, KV8, true>) == cudaSuccess &&
+         fa.numRegs == REG_LAUNCH && fw.numRegs == REG_LAUNCH;
   }
   return ok == 1;
 }
@@ -725,21 +773,27 @@ cudaError_t launch_prefill_tc2(const AttnArgs& a, int q_dtype, int kv_dtype, int
                                cudaStream_t st) {
   if (grid_x == 0) return cudaSuccess;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
-  CUtensorMap tk, tv;
+  // boxes of one 16-token page slot, and of one 128-key tile (BN)
+  static_assert(Tc2Cfg<64, false>::BN == 128 && Tc2Cfg<128, false>::BN == 128 &&
+                    Tc2Cfg<128, true>::BN == 128,
+                "tile box");
+  CUtensorMap tk, tv, tkw, tvw;
   if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
+      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_kv_map_rows(&tkw, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens, 128) ||
+      !encode_kv_map_rows(&tvw, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens, 128))
     return cudaErrorInvalidValue;
   const bool bf = q_dtype == PA_BF16;
   if (kv_dtype == PA_E5M2) {
     if (a.p.d != 128) return cudaErrorInvalidValue;
-    return bf ? launch_tc2<__nv_bfloat16, 128, true>(a, tk, tv, grid_x, st)
-              : launch_tc2<__half, 128, true>(a, tk, tv, grid_x, st);
+    return bf ? launch_tc2<__nv_bfloat16, 128, true>(a, tk, tv, tkw, tvw, grid_x, st)
+              : launch_tc2<__half, 128, true>(a, tk, tv, tkw, tvw, grid_x, st);
   }
   switch (a.p.d) {
-    case 64: return bf ? launch_tc2<__nv_bfloat16, 64, false>(a, tk, tv, grid_x, st)
-                       : launch_tc2<__half, 64, false>(a, tk, tv, grid_x, st);
-    case 128: return bf ? launch_tc2<__nv_bfloat16, 128, false>(a, tk, tv, grid_x, st)
-                        : launch_tc2<__half, 128, false>(a, tk, tv, grid_x, st);
+    case 64: return bf ? launch_tc2<__nv_bfloat16, 64, false>(a, tk, tv, tkw, tvw, grid_x, st)
+                       : launch_tc2<__half, 64, false>(a, tk, tv, tkw, tvw, grid_x, st);
+    case 128: return bf ? launch_tc2<__nv_bfloat16, 128, false>(a, tk, tv, tkw, tvw, grid_x, st)
+                        : launch_tc2<__half, 128, false>(a, tk, tv, tkw, tvw, grid_x, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -103,6 +103,28 @@ def test_prefill_fp8_cache(dtype, d):
     assert_bitwise(outs[48], outs[16])
 
 
+@pytest.mark.parametrize("dtype,kv,d", [("bf16", None, 64), ("bf16", None, 128),
+                                        ("f16", "e5m2", 128), ("f16", None, 256),
+                                        ("bf16", None, 256), ("f16", "e5m2", 256)])
+def test_prefill_whole_tile_copies(dtype, kv, d):
+    # pages that can hold a whole 128-key tile: a tile (or V half) whose keys
+    # lie in one page is copied with one box per 128-byte chunk instead of one
+    # per 16-token slot.  Pages of 128 tokens (every full tile inside a page),
+    # 144 (tiles across page boundaries) and 784, shuffled page order, rows
+    # ending mid-slot, NaN in the unused slots: bitwise the result with
+    # 16-token pages, which is within tolerance of the oracle
+    ql, kl = [65, 300, 3, 129, 600], [65, 1500, 1, 700, 2000]
+    kw = dict(hq=8, hkv=2, d=d, dtype=dtype, kv_dtype=kv, seed=60 + d,
+              k_scale=0.37 if kv else 1.0, v_scale=1.7 if kv else 1.0)
+    cpu, gpu = small(ql, kl, P=16, **kw)
+    base = run("prefill", gpu)
+    assert max_err(base, ref_of(cpu)) <= TOL[kv or dtype]
+    for P in (128, 144, 784):
+        for perm in (None, 3):
+            _, g = small(ql, kl, P=P, perm_seed=perm, poison="nan", **kw)
+            assert_bitwise(run("prefill", g), base)
+
+
 DECODE_LENS = [0, 1, 31, 32, 33, 511, 512, 513, 4097, 10000]
 
 
