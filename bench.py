@@ -51,10 +51,10 @@ L2_BYTES = 129 * 1024 * 1024
 # only while the kernel's sources hash to the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "baf52541e5843e3bfdc1ce9db5b4f65330b86732f03196a473c3b75eef050906",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "b2748af3f6316ae4ced295102040fe58930c6820948a865949132a553af28b0f",
         "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "629b7fbaf3806ae668af86f08a63be4db05820bfc0a147133c0a08a4cf9fb924",
     },
-    "bytes_per_launch": 955248128 + 54281728,
+    "bytes_per_launch": 955822592 + 53535232,
 }
 
 
