@@ -9,8 +9,9 @@
 //  * A work item is (row, KV head, split, 16-row block of GQA-packed query
 //    rows).  Each warp takes one item at a time from a counter in the
 //    workspace and streams the item's keys in 16-token page slots: one TMA
-//    box per 128 bytes of a key row, for K and for V, straight from the
-//    block table into the warp's private ring of NS slots.  The warp keeps
+//    box per slot for K and one for V (16 keys x the whole d of one head,
+//    as 128-byte pieces), straight from the block table into the warp's
+//    private ring of NS slots.  The warp keeps
 //    NS-1 slots in flight and prefetches across item boundaries, so HBM
 //    never waits for a warp to start its next item.  Eight warps per CTA
 //    (four for 16 KB slots) give each SM sub-partition two independent
@@ -45,6 +46,11 @@
 namespace pa {
 bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
                    int64_t tokens);
+
+// The cache as (128-byte piece, token, piece index, head) with boxes of one
+// 16-token page slot of one head, every piece: [piece][16 keys][128 B].
+bool encode_slot_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                     int64_t tokens);
 
 namespace {
 
@@ -314,11 +320,9 @@ __global__ void __launch_bounds__(DecCfg<D, KV8>::W * 32, 1)
           meta[s] = make_int2(cur_id, cur_chunk);
           mbar_arrive_expect_tx(bar, C::SLOT);
           const uint32_t dK = wring + s * C::SLOT, dV = dK + C::HALF;
-#pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(dK + c * 2048, &tmK, c * (128 / C::ELT), cur.kh, tok0, bar);
-            tma_load_3d(dV + c * 2048, &tmV, c * (128 / C::ELT), cur.kh, tok0, bar);
-          }
+          // one box per half: all NCH 128-byte chunks of the slot's 16 keys
+          tma_load_4d(dK, &tmK, 0, tok0, 0, cur.kh, bar);
+          tma_load_4d(dV, &tmV, 0, tok0, 0, cur.kh, bar);
         }
       }
       poff += 16;
@@ -755,8 +759,8 @@ cudaError_t launch_decode_tma(const AttnArgs& a, int q_dtype, int kv_dtype, int 
   if (items >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int64_t tokens = (int64_t)a.p.num_pages * a.p.page_size;
   CUtensorMap tk, tv;
-  if (!encode_kv_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
-      !encode_kv_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
+  if (!encode_slot_map(&tk, a.kc, kv_dtype, a.p.d, a.p.hkv, tokens) ||
+      !encode_slot_map(&tv, a.vc, kv_dtype, a.p.d, a.p.hkv, tokens))
     return cudaErrorInvalidValue;
   uint32_t* counters = reinterpret_cast<WsHeader*>(a.p.err)->pad;
   const bool kv8 = kv_dtype == PA_E5M2;

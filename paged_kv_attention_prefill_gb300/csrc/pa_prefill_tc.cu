@@ -1190,6 +1190,28 @@ bool encode_kv_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int 
   return encode_kv_map_rows(tm, cache, kv_dtype, d, hkv, tokens, 16);
 }
 
+// [tokens, Hkv, d] cache viewed as (128-byte piece, token, piece index, head)
+// with boxes of (128 bytes, 16 tokens, all d / 128 pieces, 1 head): one copy
+// lands a 16-token page slot of one head as [piece][16 keys][128 B], 128-byte
+// swizzle -- the layout of a decode ring slot half.
+bool encode_slot_map(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
+                     int64_t tokens) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int elt = kv_dtype == PA_E5M2 ? 1 : 2;
+  const int per = 128 / elt, pieces = d * elt / 128;
+  cuuint64_t dims[4] = {(cuuint64_t)per, (cuuint64_t)tokens, (cuuint64_t)pieces, (cuuint64_t)hkv};
+  cuuint64_t strides[3] = {(cuuint64_t)hkv * d * elt, 128, (cuuint64_t)d * elt};
+  cuuint32_t box[4] = {(cuuint32_t)per, 16, (cuuint32_t)pieces, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType dt = kv_dtype == PA_E5M2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : kv_dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return fn(tm, dt, 4, const_cast<void*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 template <typename T>
