@@ -89,6 +89,11 @@ __host__ __device__ inline int dec_num_splits(int L, int by_len) {
 __host__ __device__ inline bool dec_is_long(int L, int by_len) {
   return by_len && L > LONG_MIN_TILES * DEC_KT;
 }
+// "Last visible key" of a padding row of a query tile (past the row's
+// queries): no key is masked, so its warps never take the diagonal path on
+// every tile.  Its logits are finite (its Q is zero and the keys past a row's
+// end are zero-filled) and its outputs are never stored.
+constexpr int NO_MASK = 1 << 30;
 constexpr int DEC_ROWS = 16;    // GQA-packed query rows per decode CTA
 constexpr int PF_BM = 64;       // GQA-packed query rows per prefill CTA (mma.sync path)
 

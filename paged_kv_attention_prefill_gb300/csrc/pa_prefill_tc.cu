@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
     // last visible key, from k0 (a decode split also ends at k1)
-    const int last = valid ? min(L - qb + i, k1 - 1) - k0 : -1 - k0;
+    const int last = valid ? min(L - qb + i, k1 - 1) - k0 : NO_MASK;
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     {
@@ -960,7 +960,7 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
     const int R = R0 + r;
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
-    const int last = valid ? L - qb + i - k0 : -1 - k0;  // last visible key, from k0
+    const int last = valid ? L - qb + i - k0 : NO_MASK;  // last visible key, from k0
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
     const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
     {

@@ -549,7 +549,7 @@ __global__ void __launch_bounds__(384, 1)
     const bool valid = R < M;
     const int i = valid ? R / g : 0, hg = valid ? R % g : 0;
     // last visible key of this row, counted from the start of the key range
-    const int last = valid ? L - qb + i - k0 : -1 - k0;
+    const int last = valid ? L - qb + i - k0 : NO_MASK;
     const int64_t qoff = ((int64_t)(qs + i) * p.hq + kh * g + hg) * D;
     const int n = t ? nB : nA;
     const uint32_t q_t = sQ + t * C::Q_BYTES;
