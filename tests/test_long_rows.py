@@ -211,3 +211,27 @@ def test_workload5_by_length_sampled():
     assert same_bits(run("decode", b, host=False, num_splits=BY_LEN), out)
     del b
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case", ["tile_f16_d256", "decode_e5m2_d128"])
+def test_rows_past_the_part_cap(case):
+    # rows over 262144 keys: at most 128 parts, so the parts grow past 2048
+    # keys (whole 128-key tiles); sampled tokens against the oracle, bitwise
+    # without host mirrors and row alone vs in the batch
+    if case == "tile_f16_d256":
+        kw = dict(dtype="f16", d=256, hq=8, hkv=2)
+        tol = TOL["f16"]
+    else:
+        kw = dict(dtype="bf16", d=128, hq=8, hkv=2, kv_dtype="e5m2", k_scale=0.37, v_scale=1.7)
+        tol = 2e-2
+    q_lens, kv_lens = [1, 4, 1], [300000, 270001, 5000]
+    b = batch(q_lens, kv_lens, seed=47, **kw)
+    out = run("decode", b, num_splits=BY_LEN)
+    toks = [0, 1, 4, 5]
+    ref = oracle.paged_attention(tokens=toks, **b.oracle_args())
+    assert max_err(out[toks], ref) <= tol
+    assert same_bits(run("decode", b, host=False, num_splits=BY_LEN), out)
+    alone = run("decode", workloads.sub_batch(b, [1], device="cuda"), num_splits=BY_LEN)
+    assert same_bits(alone, out[1:5])
+    del b
+    torch.cuda.empty_cache()
