@@ -742,7 +742,8 @@ __global__ void __launch_bounds__(Tc8Cfg::THREADS, 1)
   if (warp == 0 || warp == 2) {
     // ===== warp 0 streams the K codes of each key tile (128 keys), warp 2 ==
     // the V codes in 64-key halves, into the code rings: one TMA box (16
-    // keys x 128 codes) per page slot and 128-code chunk of the row; the slot
+    // keys x 128 codes) per page slot and 128-code chunk of the row (with
+    // pages of 128 tokens or more, one per chunk of a unit in one page); the slot
     // holding the row's last key is copied by hand, zero-filled past the
     // row's end.  Two warps, so that a ring waiting for its stage to be
     // widened never holds back the other ring's requests (the codes take
@@ -1166,8 +1167,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// [tokens, Hkv, d] view of a cache, boxes of 16 tokens x 1 head x 128 bytes
-// (64 16-bit elements or 128 fp8 codes), 128-byte swizzle.
+// [tokens, Hkv, d] view of a cache, boxes of `rows` tokens x 1 head x 128
+// bytes (64 16-bit elements or 128 fp8 codes), 128-byte swizzle: 16 rows for
+// one page slot, a whole key tile or V half for the large-page kernels.
 bool encode_kv_map_rows(CUtensorMap* tm, const void* cache, int kv_dtype, int d, int hkv,
                         int64_t tokens, int rows) {
   auto fn = encode_fn();

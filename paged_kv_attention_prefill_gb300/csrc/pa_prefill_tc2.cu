@@ -205,8 +205,9 @@ __global__ void __launch_bounds__(384, 1)
     setmaxnreg_dec<reg_low(KV8)>();
     if (KV8 && warp == 0) {
       // ===== fp8 cache: warp 0 streams the K and V codes of each key tile ======
-      // into the code rings, one TMA box (16 keys x 128 codes) per page slot;
-      // the slot holding the row's last key is copied by hand, zero-filled.
+      // into the code rings, one TMA box (16 keys x 128 codes) per page slot
+      // (with pages of 128 tokens or more, one per tile in one page); the
+      // slot holding the row's last key is copied by hand, zero-filled.
       const uint8_t* kc8 = static_cast<const uint8_t*>(a.kc);
       const uint8_t* vc8 = static_cast<const uint8_t*>(a.vc);
       if (lane == 0) {
