@@ -51,7 +51,7 @@ L2_BYTES = 129 * 1024 * 1024
 # only while the kernel's sources hash to the ones that were profiled.
 PROFILED_PREFILL_TRAFFIC = {
     "sources": {
-        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "9621201d18e911ec0dd386da7bf87d9642567a61485c48eb934cfac8cd07155e",
+        "paged_kv_attention_prefill_gb300/csrc/pa_prefill_tc2.cu": "a5b45c33948c01dfe93911f7a6286ed1a0308b74000aad8c1c5e87f4881de834",
         "paged_kv_attention_prefill_gb300/csrc/pa_sm100.cuh": "7d06c7946e0693914ca226a6d0f71e3825078c65055e4edd196bfeb33a533b84",
         "paged_kv_attention_prefill_gb300/csrc/pa_internal.cuh": "a83b5cf1cddace0bea41b9a50005ac4c9176cdee12d0c0315dbf0d09448b1988",
     },
