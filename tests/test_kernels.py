@@ -125,6 +125,29 @@ def test_prefill_whole_tile_copies(dtype, kv, d):
             assert_bitwise(run("prefill", g), base)
 
 
+@pytest.mark.parametrize("dtype,kv,d", [("bf16", None, 128), ("f16", "e5m2", 128),
+                                        ("f16", None, 256), ("f16", "e5m2", 256)])
+def test_whole_tile_copies_with_key_range_parts(dtype, kv, d):
+    # key-range parts (whole 128-key units) start their copies mid-row: with
+    # pages of 256 and 784 tokens the parts' tiles take the whole-tile boxes
+    # where they lie in one page; bitwise the 16-token-page result, itself
+    # within tolerance of the oracle; and a mixed call (decode rows beside the
+    # cut prefill rows) bitwise its single-path calls
+    ql, kl = [700, 1, 4, 300], [9000, 3000, 2500, 6000]
+    kw = dict(hq=8, hkv=2, d=d, dtype=dtype, kv_dtype=kv, seed=90 + d,
+              k_scale=0.37 if kv else 1.0, v_scale=1.7 if kv else 1.0)
+    cpu, gpu = small(ql, kl, P=16, **kw)
+    base = run("mixed", gpu, prefill_kv_parts=3)
+    toks = [0, 350, 699, 700, 701, 705, 1004]
+    assert max_err(base[toks], ref_of(cpu, toks)) <= TOL[kv or dtype]
+    for P in (256, 784):
+        _, g = small(ql, kl, P=P, perm_seed=9, **kw)
+        assert_bitwise(run("mixed", g, prefill_kv_parts=3), base)
+    pre = run("prefill", workloads.sub_batch(cpu, [0, 3]).to("cuda"), prefill_kv_parts=3)
+    assert_bitwise(base[:700], pre[:700])
+    assert_bitwise(base[705:], pre[700:])
+
+
 DECODE_LENS = [0, 1, 31, 32, 33, 511, 512, 513, 4097, 10000]
 
 
