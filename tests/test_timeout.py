@@ -62,15 +62,15 @@ def flags(lib, ws):
     return int(v.value)
 
 
-def make(q_lens, kv_lens, d, dtype="bf16", kv_dtype=None, hq=8, hkv=2, seed=50, **kw):
+def make(q_lens, kv_lens, d, dtype="bf16", kv_dtype=None, hq=8, hkv=2, seed=50, P=16, **kw):
     return workloads.make_batch(q_lens, kv_lens, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
-                                page_size=16, q_dtype=dtype, kv_dtype=kv_dtype, seed=seed,
+                                page_size=P, q_dtype=dtype, kv_dtype=kv_dtype, seed=seed,
                                 device="cuda", **kw)
 
 
 # (entry, batch, params): the two-tile prefill (16-bit and fp8 caches), the
-# one-tile d = 256 prefill (16-bit and fp8), the TMA decode, and the long-row
-# decode splits on the tile kernel
+# one-tile d = 256 prefill (16-bit and fp8), the TMA decode, the long-row
+# decode splits on the tile kernel, and the large-page instances
 CASES = {
     "prefill_d128": ("paged_attn_prefill", lambda: make([300, 200], [3000, 2500], 128), {}),
     "prefill_d128_fp8": ("paged_attn_prefill",
@@ -85,6 +85,18 @@ CASES = {
     "decode_long_d256": ("paged_attn_decode", lambda: make([1, 4], [40000, 34000], 256, "f16",
                                                           hq=12),
                          {"num_splits": pa.PA_SPLITS_BY_LENGTH}),
+    # the large-page instances (a key tile in one page copied in one box per
+    # chunk)
+    "prefill_d128_pages256": ("paged_attn_prefill", lambda: make([300, 200], [3000, 2500], 128,
+                                                                 P=256), {}),
+    "prefill_d256_pages784": ("paged_attn_prefill", lambda: make([200], [3000], 256, "f16",
+                                                                 hq=12, P=784), {}),
+    "prefill_d256_fp8_pages784": ("paged_attn_prefill",
+                                  lambda: make([200], [3000], 256, "f16", "e5m2", hq=12,
+                                               k_scale=0.5, v_scale=2.0, P=784), {}),
+    "decode_long_d256_pages784": ("paged_attn_decode",
+                                  lambda: make([1, 4], [40000, 34000], 256, "f16", hq=12, P=784),
+                                  {"num_splits": pa.PA_SPLITS_BY_LENGTH}),
 }
 
 
